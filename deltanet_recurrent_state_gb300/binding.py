@@ -1,0 +1,193 @@
+"""Thin ctypes binding of libdn.so (include/dn.h) for torch tensors.
+
+Argument marshalling only: shapes, dtypes and devices are checked, raw device
+pointers and the current CUDA stream are passed to the C ABI, and a non-OK
+status raises ``DnError``. Every step of the computation runs in the library's
+CUDA kernels; there is no other implementation to fall back to, so a missing
+library raises at load time.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdn.so")
+
+DN_OK, DN_ERR_INVALID_ARG, DN_ERR_UNSUPPORTED, DN_ERR_CUDA = 0, 1, 2, 3
+DN_F16, DN_F32 = 0, 1
+MAX_BLOCK = 16
+PREFILL_CHUNK = 64
+
+_DT = {torch.float16: DN_F16, torch.float32: DN_F32}
+
+# Every exported symbol of include/dn.h with its ctypes signature.
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "dn_verify_block": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dn_accept_workspace_bytes": (_S, [_I, _I, _I]),
+    "dn_accept_greedy": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
+    "dn_commit": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "dn_prefill_checkpoint": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _P, _P]),
+    "dn_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class DnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = load_library().dn_status_string(status).decode()
+        super().__init__("%s failed: %s" % (fn, msg))
+
+
+_lib = None
+
+
+def load_library(path=None):
+    """Load libdn.so (once) and declare the C signatures. Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            "libdn.so is not built (%s); build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`" % p)
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(name, status):
+    if status != DN_OK:
+        raise DnError(name, status)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("all tensors must be CUDA tensors")
+            if not t.is_contiguous():
+                raise ValueError("all tensors must be contiguous")
+
+
+def dn_verify_block(q, k, v, beta, g, state_in, out=None, ckpt=None, stream=None):
+    """q, k [N,T,H,dk]; v [N,T,H,dv]; beta, g [N,T,H] fp32; state_in [N,H,dv,dk].
+
+    Returns (out [N,T,H,dv], ckpt [N,T,H,dv,dk]); allocates them with torch if not given.
+    """
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
+    if ckpt is None:
+        ckpt = torch.empty((N, T, H, dv, dk), dtype=state_in.dtype, device=q.device)
+    _dev(q, k, v, beta, g, state_in, out, ckpt)
+    assert k.shape == q.shape and v.shape == (N, T, H, dv)
+    assert beta.shape == (N, T, H) and g.shape == (N, T, H)
+    assert beta.dtype == torch.float32 and g.dtype == torch.float32
+    assert state_in.shape == (N, H, dv, dk) and ckpt.shape == (N, T, H, dv, dk)
+    assert out.shape == (N, T, H, dv) and out.dtype == q.dtype and ckpt.dtype == state_in.dtype
+    st = load_library().dn_verify_block(
+        N, H, T, dk, dv, _DT[q.dtype], _DT[state_in.dtype], _ptr(q), _ptr(k), _ptr(v),
+        _ptr(beta), _ptr(g), _ptr(state_in), _ptr(out), _ptr(ckpt), _stream(stream))
+    _check("dn_verify_block", st)
+    return out, ckpt
+
+
+def dn_accept_workspace_bytes(B, T, V):
+    return int(load_library().dn_accept_workspace_bytes(B, T, V))
+
+
+def accept_workspace(B, T, V, device):
+    """A zeroed workspace of dn_accept_workspace_bytes(B, T, V) bytes."""
+    n = dn_accept_workspace_bytes(B, T, V)
+    return torch.zeros((max(n, 16),), dtype=torch.uint8, device=device)
+
+
+def dn_accept_greedy(logits, draft_ids, target_ids=None, accepted_len=None, workspace=None,
+                     stream=None):
+    """logits [B,T,V] fp16/fp32, draft_ids [B,T] int32 -> (target_ids [B,T], accepted_len [B])."""
+    B, T, V = logits.shape
+    dev = logits.device
+    if target_ids is None:
+        target_ids = torch.empty((B, T), dtype=torch.int32, device=dev)
+    if accepted_len is None:
+        accepted_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = accept_workspace(B, T, V, dev)
+    _dev(logits, draft_ids, target_ids, accepted_len, workspace)
+    assert draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32
+    assert target_ids.shape == (B, T) and accepted_len.shape == (B,)
+    st = load_library().dn_accept_greedy(
+        B, T, V, _DT[logits.dtype], _ptr(logits), _ptr(draft_ids), _ptr(target_ids),
+        _ptr(accepted_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check("dn_accept_greedy", st)
+    return target_ids, accepted_len
+
+
+def dn_commit(ckpt, accepted_len, state, stream=None):
+    """ckpt [N,T,H,dv,dk], accepted_len [B] int32 (device), state [N,H,dv,dk] updated in place."""
+    N, H, dv, dk = state.shape
+    T = ckpt.shape[1]
+    B = accepted_len.shape[0]
+    _dev(ckpt, accepted_len, state)
+    assert ckpt.shape == (N, T, H, dv, dk) and ckpt.dtype == state.dtype
+    assert accepted_len.dtype == torch.int32
+    st = load_library().dn_commit(N, B, H, T, dk, dv, _DT[state.dtype], _ptr(ckpt),
+                                  _ptr(accepted_len), _ptr(state), _stream(stream))
+    _check("dn_commit", st)
+    return state
+
+
+def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, state_out=None,
+                          chunk=PREFILL_CHUNK, state_dtype=None, stream=None):
+    """q, k [N,P,H,dk]; v [N,P,H,dv]; beta, g [N,P,H]; state_in [N,H,dv,dk] or None.
+
+    Returns (out [N,P,H,dv], ckpt [N,P//chunk,H,dv,dk], state_out [N,H,dv,dk]).
+    """
+    N, P, H, dk = q.shape
+    dv = v.shape[-1]
+    sdt = state_in.dtype if state_in is not None else (state_dtype or q.dtype)
+    dev = q.device
+    if out is None:
+        out = torch.empty((N, P, H, dv), dtype=q.dtype, device=dev)
+    if ckpt is None:
+        ckpt = torch.empty((N, P // chunk, H, dv, dk), dtype=sdt, device=dev)
+    if state_out is None:
+        state_out = torch.empty((N, H, dv, dk), dtype=sdt, device=dev)
+    _dev(q, k, v, beta, g, state_in, out, ckpt, state_out)
+    assert k.shape == q.shape and v.shape == (N, P, H, dv) and beta.shape == (N, P, H)
+    assert g.shape == (N, P, H) and out.shape == (N, P, H, dv)
+    assert ckpt.shape == (N, P // chunk, H, dv, dk) and state_out.shape == (N, H, dv, dk)
+    st = load_library().dn_prefill_checkpoint(
+        N, H, P, chunk, dk, dv, _DT[q.dtype], _DT[sdt], _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+        _ptr(g), _ptr(state_in), _ptr(out), _ptr(ckpt) if ckpt.numel() else None,
+        _ptr(state_out), _stream(stream))
+    _check("dn_prefill_checkpoint", st)
+    return out, ckpt, state_out
+
+
+def dn_status_string(status):
+    return load_library().dn_status_string(int(status)).decode()

@@ -1,0 +1,199 @@
+// dn_accept_greedy: greedy verification of B draft blocks in one launch.
+//
+// Greedy verify ("Qwen3.8-27B on a Single RTX 3090: ...", Technical Insight,
+// split-KV verify): the target token at each position is the argmax of its
+// logits row, and the accepted length is the longest prefix on which the drafts
+// equal the targets.
+//
+// One pass over the logits. Grid = (chunks of kChunk vocab entries) x (B*T rows).
+// Each CTA reduces its chunk to one 64-bit key, (order-preserving value bits << 32)
+// | (0xffffffff - index), so an unsigned max picks the largest value and, among
+// equal values, the lowest index; the order of the reduction cannot change the
+// answer. The last CTA of a row (found with a counter in the workspace) reduces
+// the row's chunk keys and writes the target id; the last row of a request then
+// computes the accepted length. Both counters are reset by the CTA that finishes
+// them, so the workspace is ready for the next call. Nothing spins or waits.
+#include <cuda_runtime.h>
+
+#include "dn.h"
+#include "dn_internal.h"
+
+namespace dn {
+namespace {
+
+constexpr int kChunk = 8192;   // vocab entries per CTA
+constexpr int kThreads = 256;
+
+__host__ __device__ inline int accept_chunks(int V) { return (V + kChunk - 1) / kChunk; }
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+struct AcceptWorkspace {
+    unsigned long long *keys;   // [rows][chunks]
+    unsigned int *row_count;    // [rows]
+    unsigned int *req_count;    // [B]
+};
+
+__host__ __device__ inline size_t accept_ws_bytes(int B, int T, int V) {
+    const size_t rows = (size_t)B * T;
+    return align16(rows * accept_chunks(V) * sizeof(unsigned long long)) +
+           align16(rows * sizeof(unsigned int)) + align16((size_t)B * sizeof(unsigned int));
+}
+
+__host__ __device__ inline AcceptWorkspace accept_ws(void *base, int B, int T, int V) {
+    const size_t rows = (size_t)B * T;
+    char *p = static_cast<char *>(base);
+    AcceptWorkspace w;
+    w.keys = reinterpret_cast<unsigned long long *>(p);
+    p += align16(rows * accept_chunks(V) * sizeof(unsigned long long));
+    w.row_count = reinterpret_cast<unsigned int *>(p);
+    p += align16(rows * sizeof(unsigned int));
+    w.req_count = reinterpret_cast<unsigned int *>(p);
+    return w;
+}
+
+// Order-preserving maps of the value bits to unsigned integers (finite inputs).
+// -0.0 is folded onto +0.0 first, so the two compare equal as numbers do.
+__device__ __forceinline__ unsigned int order_key(unsigned short h) {
+    if ((h & 0x7fffu) == 0) h = 0;
+    return (h & 0x8000u) ? (unsigned int)(~h & 0xffffu) : (unsigned int)(h | 0x8000u);
+}
+__device__ __forceinline__ unsigned int order_key(unsigned int f) {
+    if ((f & 0x7fffffffu) == 0) f = 0;
+    return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long pack_key(unsigned int key, int idx) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - (unsigned int)idx);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+__device__ __forceinline__ unsigned long long block_max(unsigned long long x, unsigned long long *red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = umax64(x, __shfl_xor_sync(0xffffffffu, x, off));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        x = lane < kThreads / 32 ? red[lane] : 0ull;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) x = umax64(x, __shfl_xor_sync(0xffffffffu, x, off));
+    }
+    return x;  // valid in warp 0
+}
+
+// Element bits type -> elements per 16-byte vector
+template <typename E> struct Bits;
+template <> struct Bits<unsigned short> { static constexpr int kVec = 8; };
+template <> struct Bits<unsigned int> { static constexpr int kVec = 4; };
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads)
+accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
+                     const int *__restrict__ draft, int *__restrict__ target,
+                     int *__restrict__ accepted, AcceptWorkspace ws) {
+    constexpr int VEC = Bits<E>::kVec;
+    __shared__ unsigned long long red[kThreads / 32];
+    __shared__ int is_last;
+    const int chunks = gridDim.x;
+    const int c = blockIdx.x;
+    const int row = blockIdx.y;
+    const E *rp = logits + (size_t)row * V;
+    const int c0 = c * kChunk;
+    const int c1 = min(V, c0 + kChunk);
+
+    unsigned long long best = 0ull;
+    // 16-byte vector loads where the row stays 16-byte aligned, scalar otherwise.
+    const bool vec_ok = ((size_t)V * sizeof(E)) % 16 == 0;
+    int done = c0;
+    if (vec_ok) {
+        const int nvec = (c1 - c0) / VEC;
+        const uint4 *vp = reinterpret_cast<const uint4 *>(rp + c0);
+        for (int i = threadIdx.x; i < nvec; i += kThreads) {
+            const uint4 u = __ldcs(vp + i);
+            const E *e = reinterpret_cast<const E *>(&u);
+            const int base = c0 + i * VEC;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) best = umax64(best, pack_key(order_key(e[j]), base + j));
+        }
+        done = c0 + nvec * VEC;
+    }
+    for (int i = done + threadIdx.x; i < c1; i += kThreads)
+        best = umax64(best, pack_key(order_key(rp[i]), i));
+    best = block_max(best, red);
+
+    if (threadIdx.x == 0) {
+        ws.keys[(size_t)row * chunks + c] = best;
+        __threadfence();
+        const unsigned int prev = atomicAdd(&ws.row_count[row], 1u);
+        is_last = (prev == (unsigned int)chunks - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+
+    // Last CTA of this row: reduce the row's chunk keys.
+    __threadfence();
+    unsigned long long k = 0ull;
+    for (int i = threadIdx.x; i < chunks; i += kThreads)
+        k = umax64(k, __ldcg(&ws.keys[(size_t)row * chunks + i]));
+    k = block_max(k, red);
+    if (threadIdx.x == 0) {
+        const int tgt = (int)(0xffffffffu - (unsigned int)(k & 0xffffffffull));
+        target[row] = tgt;
+        ws.row_count[row] = 0u;
+        __threadfence();
+        const int b = row / T;
+        const unsigned int prev = atomicAdd(&ws.req_count[b], 1u);
+        if (prev == (unsigned int)T - 1) {
+            // Last row of request b: every target of b is written and visible.
+            __threadfence();
+            int a = T;
+            for (int t = 0; t < T; ++t) {
+                if (__ldcg(&draft[b * T + t]) != __ldcg(&target[b * T + t])) {
+                    a = t;
+                    break;
+                }
+            }
+            accepted[b] = a;
+            ws.req_count[b] = 0u;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace dn
+
+extern "C" size_t dn_accept_workspace_bytes(int B, int T, int V) {
+    if (B < 1 || T < 1 || V < 1) return 0;
+    return dn::accept_ws_bytes(B, T, V);
+}
+
+extern "C" dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, const void *logits,
+                                      const int32_t *draft_ids, int32_t *target_ids,
+                                      int32_t *accepted_len, void *workspace,
+                                      size_t workspace_bytes, dn_stream_t stream) {
+    using namespace dn;
+    if (B < 0 || T < 1 || V < 1 || !dtype_ok(logit_dt)) return DN_ERR_INVALID_ARG;
+    if ((long long)B * T > 65535) return DN_ERR_INVALID_ARG;  // grid.y limit
+    if (B == 0) return DN_OK;
+    if (!logits || !draft_ids || !target_ids || !accepted_len || !workspace) return DN_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(draft_ids, 4) || !aligned(target_ids, 4) ||
+        !aligned(accepted_len, 4) || !aligned(workspace, 16))
+        return DN_ERR_INVALID_ARG;
+    if (workspace_bytes < accept_ws_bytes(B, T, V)) return DN_ERR_INVALID_ARG;
+    const AcceptWorkspace ws = accept_ws(workspace, B, T, V);
+    const dim3 grid(accept_chunks(V), B * T);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (logit_dt == DN_F16)
+        accept_greedy_kernel<unsigned short><<<grid, kThreads, 0, st>>>(
+            B, T, V, static_cast<const unsigned short *>(logits), draft_ids, target_ids,
+            accepted_len, ws);
+    else
+        accept_greedy_kernel<unsigned int><<<grid, kThreads, 0, st>>>(
+            B, T, V, static_cast<const unsigned int *>(logits), draft_ids, target_ids,
+            accepted_len, ws);
+    return launch_status();
+}

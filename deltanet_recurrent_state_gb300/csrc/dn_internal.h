@@ -1,0 +1,29 @@
+// Host-side helpers shared by the entry points of libdn.so: argument checks and
+// launch-error mapping. Nothing here touches the GPU except launch_status.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dn.h"
+
+namespace dn {
+
+inline bool aligned(const void *p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+inline size_t dtype_bytes(dn_dtype t) { return t == DN_F16 ? 2 : 4; }
+
+inline bool dtype_ok(dn_dtype t) { return t == DN_F16 || t == DN_F32; }
+
+// After a launch: map a launch failure to DN_ERR_CUDA (and clear it).
+inline dn_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? DN_OK : DN_ERR_CUDA;
+}
+
+}  // namespace dn

@@ -1,0 +1,215 @@
+/*
+ * dn.h -- C ABI of libdn.so, the GB300 (sm_103a) DeltaNet recurrent-state path.
+ *
+ * Four operations make up the path a hybrid DeltaNet model runs for every
+ * speculative verify step and every prompt:
+ *
+ *   dn_verify_block        run the draft block through the recurrence, keep one
+ *                          state checkpoint per position
+ *   dn_accept_greedy       argmax of each position's logits, longest matching
+ *                          draft prefix
+ *   dn_commit              make the checkpoint at the accepted position the
+ *                          request's state (or keep the state when nothing was
+ *                          accepted)
+ *   dn_prefill_checkpoint  run a prompt through the recurrence and checkpoint the
+ *                          state every `chunk` tokens for prefix caching
+ *
+ * The recurrence is the gated delta rule (Yang, Kautz, Hatamizadeh 2024,
+ * "Gated Delta Networks"), the DeltaNet layer the pages serve:
+ *
+ *     S_t = g_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t q_t
+ *
+ * S is a dv x dk matrix per (state set, head). A "state set" is one request's
+ * state in one layer; callers may fold several layers of one request (or
+ * several requests) into the leading dimension N of one call.
+ *
+ * LAYOUT. Every array is dense row-major (last index fastest), in device
+ * memory, with the shapes given per function. The state is stored as the math
+ * S itself: element (i, j) of a [dv][dk] tile, i over dv, j over dk.
+ *
+ * DTYPES. Two combinations are supported: io_dt = state_dt = DN_F16 (fp16
+ * q/k/v/out and fp16 state, the 16-bit DeltaNet state of the pages) and
+ * io_dt = state_dt = DN_F32. beta and g are always fp32. Inside a call the
+ * state is carried in fp32; it is rounded (round-to-nearest-even) to the state
+ * dtype only where it is stored.
+ *
+ * OWNERSHIP. The library allocates nothing, keeps no state between calls and
+ * holds no pointer after a call returns. All buffers belong to the caller.
+ * Every call only enqueues work on `stream` (NULL means the legacy default
+ * stream) and returns without synchronising; results are ready when the
+ * stream reaches that point. Calls are deterministic: the same inputs give
+ * bit-identical outputs.
+ *
+ * ERRORS. Every argument is checked on the host before anything is enqueued.
+ * A malformed argument (null pointer where one is required, pointer not aligned
+ * as stated, count out of range) returns DN_ERR_INVALID_ARG; a well-formed but
+ * unsupported shape or dtype (dk or dv not 64/128, another dtype pair, another
+ * chunk size) returns DN_ERR_UNSUPPORTED. In both cases nothing is enqueued.
+ * DN_ERR_CUDA means a CUDA launch failed; the CUDA error has been consumed
+ * with cudaGetLastError. Calls with a zero-sized leading count (N = 0, B = 0)
+ * return DN_OK without enqueuing anything.
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "HyperQwen: 1,000 tok/s on a Single RTX 3090 Through Aggressive
+ *        Recurrent-State Speculation", Technical Insight.
+ *   [P2] "HyperQwen" (project README), The numbers behind that.
+ *   [P3] "Qwen3.8-27B on a Single RTX 3090: How Calibrated Quantization and
+ *        Speculative Decoding Hit 1,000 tok/s", Technical Insight.
+ *   [P4] "HyperQwen on one RTX 3090: a first-time developer's guide to the
+ *        381-token claim", What actually became faster?.
+ */
+#ifndef DN_H
+#define DN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *dn_stream_t;
+
+typedef enum {
+    DN_OK = 0,
+    DN_ERR_INVALID_ARG = 1,
+    DN_ERR_UNSUPPORTED = 2,
+    DN_ERR_CUDA = 3
+} dn_status;
+
+typedef enum { DN_F16 = 0, DN_F32 = 1 } dn_dtype;
+
+/* Largest verify block (7 model drafts + 8 context drafts + 1 [P4]). */
+#define DN_MAX_BLOCK 16
+/* The only supported prefill checkpoint interval. */
+#define DN_PREFILL_CHUNK 64
+
+/*
+ * dn_verify_block -- one verify block of T tokens, per-position checkpoints.
+ *
+ * The recurrent state of a DeltaNet layer grows with the verify width because
+ * each verified position keeps its own state copy, so that any accepted prefix
+ * can be committed ([P1]: 1.66 GiB at 15 drafts vs 0.88 GiB at 7; [P2]: a
+ * speculating request "reserves recurrent-state pages"). The block is at most
+ * 16 tokens wide ([P4]).
+ *
+ * For every state set n < N and head h < H, starting from S = state_in[n][h]:
+ *   for t = 0 .. T-1:  S = g[n][t][h] * S (I - beta[n][t][h] k k^T) + beta[n][t][h] v k^T
+ *                      out[n][t][h][:] = S q          (with k, v, q of [n][t][h])
+ *                      ckpt[n][t][h]   = S            (rounded to state_dt)
+ *
+ *   N        number of state sets (>= 0); layers of one request may be folded in
+ *   H        heads per state set (>= 1)
+ *   T        block width, 1 .. DN_MAX_BLOCK
+ *   dk, dv   key / value head dims, each 64 or 128
+ *   q, k     [N][T][H][dk]  io_dt            16-byte aligned, read only
+ *   v        [N][T][H][dv]  io_dt            16-byte aligned, read only
+ *   beta, g  [N][T][H]      fp32             4-byte aligned, read only
+ *   state_in [N][H][dv][dk] state_dt         16-byte aligned, read only
+ *   out      [N][T][H][dv]  io_dt            16-byte aligned, written
+ *   ckpt     [N][T][H][dv][dk] state_dt      16-byte aligned, written
+ * Output buffers must not overlap any input.
+ */
+dn_status dn_verify_block(int N, int H, int T, int dk, int dv,
+                          dn_dtype io_dt, dn_dtype state_dt,
+                          const void *q, const void *k, const void *v,
+                          const float *beta, const float *g,
+                          const void *state_in, void *out, void *ckpt,
+                          dn_stream_t stream);
+
+/*
+ * dn_accept_workspace_bytes -- device workspace dn_accept_greedy needs.
+ * Returns 0 for B < 1, T < 1 or V < 1.
+ */
+size_t dn_accept_workspace_bytes(int B, int T, int V);
+
+/*
+ * dn_accept_greedy -- greedy verification of B draft blocks.
+ *
+ * The verifier's logits are compared with the drafts and the accepted prefix
+ * is kept ([P3], the verify step of the split-KV attention; "roughly 15 of
+ * those 16 tokens were accepted per step" on document reproduction, [P4]):
+ *
+ *   target_ids[b][t]  = the lowest index v holding the maximum of logits[b][t][:]
+ *                       (values compared as numbers, so -0.0 ties +0.0)
+ *   accepted_len[b]   = the first t with draft_ids[b][t] != target_ids[b][t], or T
+ *
+ *   logits        [B][T][V] logit_dt (DN_F16 or DN_F32), 16-byte aligned;
+ *                 every value finite (not checked)
+ *   draft_ids     [B][T] int32, 4-byte aligned
+ *   target_ids    [B][T] int32, written
+ *   accepted_len  [B] int32, written; stays on the device (dn_commit reads it
+ *                 there, no host round trip is needed)
+ *   workspace     >= dn_accept_workspace_bytes(B, T, V) bytes, 16-byte aligned.
+ *                 It must hold zeros before its first use (cudaMemset once
+ *                 after allocating it); every call leaves it ready for the
+ *                 next one. Calls that may run concurrently need separate
+ *                 workspaces.
+ *   B >= 0, T >= 1, V >= 1, B * T <= 65535.
+ */
+dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, const void *logits,
+                           const int32_t *draft_ids, int32_t *target_ids,
+                           int32_t *accepted_len, void *workspace, size_t workspace_bytes,
+                           dn_stream_t stream);
+
+/*
+ * dn_commit -- commit or roll back each state set to its accepted position.
+ *
+ * After verification the accepted prefix is kept and the rejected drafts are
+ * discarded ([P3], verify step); for the recurrent state that means:
+ *
+ *   for n < N with a = accepted_len[n % B]:
+ *     a == 0        : state[n] unchanged
+ *     1 <= a <= T   : state[n] = ckpt[n][a-1]     (all H heads)
+ *     otherwise     : state[n] unchanged (an out-of-range length is ignored)
+ *
+ *   N multiple of B, N <= 65535; state set n belongs to request n % B (sets
+ *   laid out [layer][request], n = layer * B + request).
+ *   ckpt          [N][T][H][dv][dk] state_dt, 16-byte aligned (dn_verify_block's)
+ *   accepted_len  [B] int32 in device memory, 4-byte aligned
+ *   state         [N][H][dv][dk] state_dt, 16-byte aligned, updated in place
+ */
+dn_status dn_commit(int N, int B, int H, int T, int dk, int dv, dn_dtype state_dt,
+                    const void *ckpt, const int32_t *accepted_len, void *state,
+                    dn_stream_t stream);
+
+/*
+ * dn_prefill_checkpoint -- run P prompt tokens, checkpoint every `chunk` tokens.
+ *
+ * Prefix caching keeps the DeltaNet state next to the attention context so that
+ * a later turn restores it instead of recomputing the prompt ([P1]; a second
+ * question on a ~25,000-token document, 22.4 s -> 0.56 s to first token, [P4]).
+ *
+ * For every sequence n < N and head h < H, starting from S = state_in[n][h]
+ * (zeros when state_in is NULL):
+ *   for p = 0 .. P-1:  S = g S (I - beta k k^T) + beta v k^T;  out[n][p][h] = S q
+ *                      if (p + 1) % chunk == 0:  S = round(S);  ckpt[n][(p+1)/chunk - 1][h] = S
+ *   state_out[n][h] = round(S)
+ * where round() rounds to state_dt. The carry at every chunk end is exactly the
+ * stored checkpoint, so a run restored from ckpt[c] continues bit-identically to
+ * the full run. The tail after the last full chunk writes no checkpoint.
+ *
+ *   N >= 0 sequences of equal length P >= 0; H >= 1; chunk == DN_PREFILL_CHUNK
+ *   q, k      [N][P][H][dk] io_dt      v, out [N][P][H][dv] io_dt
+ *   beta, g   [N][P][H] fp32
+ *   state_in  [N][H][dv][dk] state_dt or NULL (zero initial state)
+ *   ckpt      [N][P / chunk][H][dv][dk] state_dt; may be NULL when P < chunk
+ *   state_out [N][H][dv][dk] state_dt; may be the same buffer as state_in
+ * Alignment as for dn_verify_block. Other outputs must not overlap any input.
+ */
+dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int dk, int dv,
+                                dn_dtype io_dt, dn_dtype state_dt,
+                                const void *q, const void *k, const void *v,
+                                const float *beta, const float *g,
+                                const void *state_in, void *out, void *ckpt,
+                                void *state_out, dn_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *dn_status_string(dn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DN_H */

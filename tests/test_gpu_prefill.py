@@ -1,0 +1,80 @@
+"""dn_prefill_checkpoint on the GPU vs the oracle, with the chunk-boundary edge cases."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deltanet_recurrent_state_gb300 import binding as dn
+from deltanet_recurrent_state_gb300 import inputs
+from tests.parity import TOL, assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("q", "k", "v", "beta", "g")
+
+
+def _case(N, P, H, d, dt, seed, with_state, cuda):
+    x = inputs.recurrence_inputs(N, P, H, d, d, io=dt, state=dt, seed=seed, device="cpu")
+    s_in = x["state"].to(cuda) if with_state else None
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k].to(cuda) for k in KEYS], s_in,
+                                                state_dtype=x["state"].dtype)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_checkpoint(*[np64(x[k]) for k in KEYS],
+                                    np64(x["state"]) if with_state else None,
+                                    chunk=64, store=dt, io=dt)
+    assert_close("out", out, ref[0], TOL[dt])
+    assert ckpt.shape[1] == P // 64
+    assert_close("ckpt", ckpt, ref[1], TOL[dt])
+    assert_close("state_out", s_out, ref[2], TOL[dt])
+    return x, out, ckpt, s_out
+
+
+@pytest.mark.parametrize("P", [0, 1, 17, 63, 64, 65, 130, 200])
+def test_fp32_d64_edges(P, cuda):
+    _case(2, P, 3, 64, "f32", 100 + P, True, cuda)
+
+
+@pytest.mark.parametrize("P", [1, 64, 129])
+@pytest.mark.parametrize("with_state", [True, False])
+def test_fp16_d128(P, with_state, cuda):
+    _case(1, P, 4, 128, "f16", 200 + P, with_state, cuda)
+
+
+def test_restore_from_checkpoint_is_bit_identical(cuda):
+    N, P, H, d = 1, 300, 4, 128
+    x = inputs.recurrence_inputs(N, P, H, d, d, seed=301, device=cuda)
+    args = [x[k] for k in KEYS]
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*args, x["state"])
+    for c in range(P // 64):
+        start = 64 * (c + 1)
+        tail = [a[:, start:].contiguous() for a in args]
+        o2, ck2, s2 = dn.dn_prefill_checkpoint(*tail, ckpt[:, c].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(s2, s_out), c
+        assert torch.equal(o2, out[:, start:]), c
+        assert torch.equal(ck2, ckpt[:, c + 1:]), c
+
+
+def test_state_out_may_alias_state_in(cuda):
+    x = inputs.recurrence_inputs(2, 100, 3, 64, 64, seed=302, device=cuda)
+    args = [x[k] for k in KEYS]
+    _, _, s_ref = dn.dn_prefill_checkpoint(*args, x["state"])
+    s = x["state"].clone()
+    dn.dn_prefill_checkpoint(*args, s, state_out=s)
+    torch.cuda.synchronize()
+    assert torch.equal(s, s_ref)
+
+
+def test_prefill_equals_verify_blocks_chained(cuda):
+    # fp32: 64 prompt tokens through prefill == four 16-token verify blocks chained
+    x = inputs.recurrence_inputs(1, 64, 2, 64, 64, io="f32", state="f32", seed=303, device=cuda)
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
+    s = x["state"]
+    for b in range(4):
+        sl = {k: x[k][:, 16 * b:16 * (b + 1)].contiguous() for k in KEYS}
+        o, c = dn.dn_verify_block(sl["q"], sl["k"], sl["v"], sl["beta"], sl["g"], s)
+        torch.testing.assert_close(o, out[:, 16 * b:16 * (b + 1)], rtol=0, atol=1e-5)
+        s = c[:, -1].contiguous()
+    torch.testing.assert_close(s, s_out, rtol=0, atol=1e-5)
+    torch.testing.assert_close(s, ckpt[:, 0], rtol=0, atol=1e-5)

@@ -1,0 +1,88 @@
+"""dn_verify_block on the GPU vs the float64 oracle, element by element.
+
+Sizes span several CTAs (dv / 32 row blocks per head, many heads and state
+sets), every block width 1..16, both head dims and both dtype pairs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deltanet_recurrent_state_gb300 import binding as dn
+from deltanet_recurrent_state_gb300 import inputs
+from tests.parity import TOL, assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_case(N, T, H, dk, dv, dt, seed, cuda):
+    x = inputs.recurrence_inputs(N, T, H, dk, dv, io=dt, state=dt, seed=seed, device="cpu")
+    g = {k: v.to(cuda) for k, v in x.items()}
+    out, ckpt = dn.dn_verify_block(g["q"], g["k"], g["v"], g["beta"], g["g"], g["state"])
+    torch.cuda.synchronize()
+    o_ref, c_ref = oracle.verify_block(np64(x["q"]), np64(x["k"]), np64(x["v"]), np64(x["beta"]),
+                                       np64(x["g"]), np64(x["state"]), store=dt, io=dt)
+    assert_close("out", out, o_ref, TOL[dt])
+    assert_close("ckpt", ckpt, c_ref, TOL[dt])
+    return out, ckpt
+
+
+def test_tiny_fp32_workload(cuda):
+    # 1 layer, 1 request, 4 heads, dk = dv = 64, T = 8, fp32 state
+    _run_case(1, 8, 4, 64, 64, "f32", 1000, cuda)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 15, 16])
+def test_fp16_d128_every_width(T, cuda):
+    _run_case(3, T, 5, 128, 128, "f16", 10 + T, cuda)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("dt", ["f16", "f32"])
+def test_mixed_head_dims(dk, dv, dt, cuda):
+    _run_case(2, 7, 3, dk, dv, dt, 20 + dk + dv, cuda)
+
+
+def test_deterministic_bitwise(cuda):
+    x = inputs.recurrence_inputs(4, 16, 6, 128, 128, seed=5, device=cuda)
+    a = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    b = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_block_equals_chained_single_token_calls(cuda):
+    # fp32: one T-wide call and T one-token calls agree within fp32 rounding
+    x = inputs.recurrence_inputs(2, 6, 3, 64, 64, io="f32", state="f32", seed=6, device=cuda)
+    out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    s = x["state"]
+    for t in range(6):
+        sl = lambda k: x[k][:, t:t + 1].contiguous()
+        o1, c1 = dn.dn_verify_block(sl("q"), sl("k"), sl("v"), sl("beta"), sl("g"), s)
+        torch.testing.assert_close(o1[:, 0], out[:, t], rtol=0, atol=1e-5)
+        torch.testing.assert_close(c1[:, 0], ckpt[:, t], rtol=0, atol=1e-5)
+        s = c1[:, 0].contiguous()
+
+
+def test_beta0_g1_leaves_state_unchanged_on_gpu(cuda):
+    x = inputs.recurrence_inputs(2, 4, 3, 128, 128, seed=7, device=cuda)
+    x["beta"].zero_()
+    x["g"].fill_(1.0)
+    _, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    torch.cuda.synchronize()
+    for t in range(4):
+        assert torch.equal(ckpt[:, t], x["state"])
+
+
+def test_outputs_do_not_spill_past_their_buffers(cuda):
+    # canaries after out and ckpt stay untouched
+    N, T, H, d = 2, 5, 3, 64
+    x = inputs.recurrence_inputs(N, T, H, d, d, seed=8, device=cuda)
+    out_buf = torch.full((N * T * H * d + 64,), 7.0, dtype=torch.float16, device=cuda)
+    ck_buf = torch.full((N * T * H * d * d + 64,), 7.0, dtype=torch.float16, device=cuda)
+    out = out_buf[:N * T * H * d].view(N, T, H, d)
+    ckpt = ck_buf[:N * T * H * d * d].view(N, T, H, d, d)
+    dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], out, ckpt)
+    torch.cuda.synchronize()
+    assert (out_buf[-64:] == 7.0).all() and (ck_buf[-64:] == 7.0).all()

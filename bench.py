@@ -1,0 +1,528 @@
+"""Benchmark of the DeltaNet verify -> accept -> commit step on one or more GB300s.
+
+One step is one pass of the decode hot path over one batch of seeded synthetic
+input, all 48 layers of a request folded into one launch per operation:
+
+    dn_verify_block (48 layers x 48 heads x 128x128 fp16 state, T = 16)
+    dn_accept_greedy (16 positions x 151,936-entry fp16 logits rows)
+    dn_commit (the checkpoint at the accepted position becomes the state)
+
+The metric counts verified token-layers (B x T x layers) per second. Inputs are
+larger than L2 and three buffer sets rotate, so no step reads what the previous
+two steps touched. Extra rows time the batch-64 step and the 25,000-token prefill.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs the same per-GPU workload on its own requests
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DeltaNet verify tokens/s (B×T×layers) on 1 GB300; achieved HBM GB/s vs peak"
+UNIT = "token-layers/s"
+HEADLINE = "single_user_l48_h48_d128_t16_f16"
+FALLBACK_HBM_GBS = 6800.0
+ROTATE = 3
+
+
+# ----------------------------------------------------------------------------- byte counts
+
+def verify_bytes(N, T, H, dk, dv, esz):
+    """Algorithmic HBM bytes of one dn_verify_block launch: read state, q, k, v, beta, g;
+    write out and T checkpoints."""
+    per_head = (dv * dk * esz + T * (2 * dk + 2 * dv) * esz + T * 8 + T * dv * dk * esz)
+    return N * H * per_head
+
+
+def accept_bytes(B, T, V, lsz):
+    return B * T * V * lsz + B * T * 8 + B * 4
+
+
+def commit_bytes(L, acc, H, dk, dv, esz):
+    """2 x one state set (read checkpoint, write state) per (layer, request) with a >= 1."""
+    return 2 * L * int((acc >= 1).sum()) * H * dv * dk * esz
+
+
+def prefill_bytes(N, P, H, dk, dv, esz, chunk=64):
+    per_head = (P * (2 * dk + 2 * dv) * esz + P * 8 + 2 * dv * dk * esz +
+                (P // chunk) * dv * dk * esz)
+    return N * H * per_head
+
+
+# ----------------------------------------------------------------------------- environment
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "deltanet_recurrent_state_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_counters.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("sources_sha256_16") != kernel_sources_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch_full")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples (200 ms) while the GPU works."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, t0, t1, gpu_index):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append(dict(ts=ts, idx=int(f[1]), sm=float(f[2]), smax=float(f[3]),
+                                 hw=f[6], hwt=f[7], swt=f[8], pcap=f[9]))
+            except Exception:
+                continue
+        idxs = sorted(set(r["idx"] for r in rows))
+        if gpu_index not in idxs and len(idxs) == 1:
+            gpu_index = idxs[0]
+        rows = [r for r in rows if r["idx"] == gpu_index]
+        win = [r for r in rows if t0 - 0.25 <= r["ts"] <= t1 + 0.25]
+        where = "timed region"
+        if not win:
+            win = [r for r in rows if r["sm"] > 0.5 * r["smax"]] or rows
+            where = "whole benchmark (timed region shorter than one sample)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in win):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in win),
+                "sm_max_mhz": max(r["smax"] for r in win), "reasons": reasons,
+                "samples": len(win), "window": where}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def make_step_sets(w, device, rank, count):
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300 import inputs
+
+    N, B, T = w["L"] * w["B"], w["B"], w["T"]
+    sets = []
+    for r in range(count):
+        seed = w["seed"] + 1000 * rank + 17 * r
+        x = inputs.recurrence_inputs(N, T, w["H"], w["dk"], w["dv"], io=w["io"], state=w["state"],
+                                     seed=seed, device=device)
+        logits, target = inputs.logits_inputs(B, T, w["V"], dtype=w["logit_dtype"],
+                                              std=w["logit_std"], seed=seed + 1, device=device)
+        acc = inputs.accepted_lengths(B, T, w["accept"], seed=seed + 2, value=w.get("accept_value"))
+        draft = inputs.draft_ids(target, acc, w["V"], seed=seed + 3)
+        x.update(logits=logits, draft=draft, acc_plan=acc)
+        x["out"] = torch.empty((N, T, w["H"], w["dv"]), dtype=x["q"].dtype, device=device)
+        x["ckpt"] = torch.empty((N, T, w["H"], w["dv"], w["dk"]), dtype=x["state"].dtype,
+                                device=device)
+        x["tgt"] = torch.empty((B, T), dtype=torch.int32, device=device)
+        x["acc"] = torch.empty((B,), dtype=torch.int32, device=device)
+        x["ws"] = dn.accept_workspace(B, T, w["V"], device)
+        sets.append(x)
+    return sets
+
+
+def run_step(x, stream, evs=None):
+    from deltanet_recurrent_state_gb300 import binding as dn
+    if evs:
+        evs[0].record(stream)
+    dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"], x["ckpt"],
+                       stream=stream)
+    if evs:
+        evs[1].record(stream)
+    dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+    if evs:
+        evs[2].record(stream)
+    dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
+    if evs:
+        evs[3].record(stream)
+
+
+def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True):
+    """Warm up, then time exactly `steps` steps between barriers; returns (seconds,
+    per-kernel mean ms [verify, accept, commit])."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            run_step(sets[i % len(sets)], stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)] \
+        if per_kernel else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            run_step(sets[i % len(sets)], stream, evs[i] if evs else None)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    secs = start.elapsed_time(end) / 1e3
+    per = None
+    if evs:
+        per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(3)]
+    return secs, per, (t_wall0, t_wall1)
+
+
+def e2e_steps(w, sets, steps, warmup, stream, device):
+    """The same step through the public API with host inputs: every step copies its
+    inputs from pinned host memory and reads its results back (out, target ids,
+    accepted length) before the next step starts."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    in_keys = ("q", "k", "v", "beta", "g", "logits", "draft")
+    host = [{k: x[k].cpu().pin_memory() for k in in_keys} for x in sets]
+    outs = [{k: torch.empty(x[k].shape, dtype=x[k].dtype).pin_memory() for k in ("out", "tgt", "acc")}
+            for x in sets]
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in in_keys)
+    d2h = sum(outs[0][k].numel() * outs[0][k].element_size() for k in outs[0])
+
+    def one(i):
+        x, h, o = sets[i % len(sets)], host[i % len(sets)], outs[i % len(sets)]
+        with torch.cuda.stream(stream):
+            for k in in_keys:
+                x[k].copy_(h[k], non_blocking=True)
+            dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                               x["ckpt"], stream=stream)
+            dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"],
+                                stream=stream)
+            dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
+            for k in ("out", "tgt", "acc"):
+                o[k].copy_(x[k], non_blocking=True)
+        stream.synchronize()
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    torch.cuda.synchronize()
+    return time.perf_counter() - t0, h2d, d2h
+
+
+def prefill_row(device, stream, layers_timed=48, reps=2):
+    """48 per-layer launches of the 25,000-token prefill (two layer buffers rotate)."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300 import inputs
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS["prefill_p25000_l48_h48_d128_c64_f16"]
+    P, H, d = w["P"], w["H"], w["dk"]
+    bufs = []
+    for r in range(2):
+        x = inputs.recurrence_inputs(1, P, H, d, d, seed=w["seed"] + r, device=device)
+        x["out"] = torch.empty((1, P, H, d), dtype=torch.float16, device=device)
+        x["ckpt"] = torch.empty((1, P // 64, H, d, d), dtype=torch.float16, device=device)
+        x["s_out"] = torch.empty((1, H, d, d), dtype=torch.float16, device=device)
+        bufs.append(x)
+
+    def layer(i):
+        x = bufs[i % 2]
+        dn.dn_prefill_checkpoint(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                                 x["ckpt"], x["s_out"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            layer(i)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(layers_timed):
+                layer(i)
+        e.record(stream)
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e) / 1e3)
+    t = min(times)
+    nbytes = prefill_bytes(1, P, H, d, d, 2) * layers_timed
+    return {"workload": "prefill_p25000_l48_h48_d128_c64_f16", "launches": layers_timed,
+            "ms_all_layers": t * 1e3, "token_layers_per_s": P * layers_timed / t,
+            "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / t / 1e9}
+
+
+def batch_row(device, stream, steps=10, warmup=3):
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS["batch64_l48_h48_d128_t4_f16"]
+    sets = make_step_sets(w, device, 0, 2)
+    secs, per, _ = timed_steps(sets, steps, warmup, stream, None)
+    N, B, T = w["L"] * w["B"], w["B"], w["T"]
+    vb = verify_bytes(N, T, w["H"], w["dk"], w["dv"], 2)
+    cb = commit_bytes(w["L"], sets[0]["acc_plan"], w["H"], w["dk"], w["dv"], 2)
+    res = {"workload": "batch64_l48_h48_d128_t4_f16", "ms_per_step": secs / steps * 1e3,
+           "token_layers_per_s": B * T * w["L"] * steps / secs,
+           "verify_ms": per[0], "verify_gbs": vb / (per[0] / 1e3) / 1e9,
+           "accept_ms": per[1], "commit_ms": per[2],
+           "commit_gbs": cb / (per[2] / 1e3) / 1e9 if per[2] > 0 else None}
+    del sets
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_inputs(w, heads, seed):
+    """One layer of workload w restricted to `heads` heads, as float64 arrays."""
+    from deltanet_recurrent_state_gb300 import inputs
+    B, T = w["B"], w["T"]
+    x = inputs.recurrence_inputs(B, T, heads, w["dk"], w["dv"], io=w["io"], state=w["state"],
+                                 seed=seed, device="cpu")
+    logits, target = inputs.logits_inputs(B, T, w["V"], dtype=w["logit_dtype"], std=w["logit_std"],
+                                          seed=seed + 1)
+    acc = inputs.accepted_lengths(B, T, w["accept"], seed=seed + 2, value=w.get("accept_value"))
+    d = {k: x[k].double().numpy() for k in ("q", "k", "v", "beta", "g", "state")}
+    d["logits"] = logits.double().numpy()
+    d["draft"] = inputs.draft_ids(target, acc, w["V"], seed=seed + 3).numpy()
+    d["heads"] = heads
+    return d
+
+
+def oracle_step(w, d):
+    """The oracle's verify + accept + commit on the sample `d`; returns (seconds,
+    token-layers), counting a layer restricted to h of H heads as h/H of a layer."""
+    import oracle
+    t0 = time.perf_counter()
+    _, ckpt = oracle.verify_block(d["q"], d["k"], d["v"], d["beta"], d["g"], d["state"],
+                                  store=w["state"], io=w["io"])
+    _, a = oracle.accept_greedy(d["logits"], d["draft"])
+    oracle.commit(d["state"], ckpt, a)
+    return time.perf_counter() - t0, w["B"] * w["T"] * d["heads"] / w["H"]
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def reference_arm(args, rank, world, budget_s=120.0):
+    """The CPU oracle, as it stands, on the same workload, metric and unit. Each step is
+    one layer of the verify step (verify + commit on a sample of heads, greedy accept over
+    the full vocabulary), with the head sample sized so the whole run stays near
+    `budget_s` seconds."""
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    if rank != 0:
+        return
+    w = WORKLOADS[HEADLINE]
+    d = oracle_inputs(w, w["H"], w["seed"])
+    t1, _ = oracle_step(w, d)
+    heads = int(max(1, min(w["H"], w["H"] * budget_s / ((args.steps + args.warmup) * t1))))
+    if heads < w["H"]:
+        d = oracle_inputs(w, heads, w["seed"])
+    for _ in range(args.warmup):
+        oracle_step(w, d)
+    total_s, total_u = 0.0, 0.0
+    for _ in range(args.steps):
+        s, u = oracle_step(w, d)
+        total_s += s
+        total_u += u
+    v = total_u / total_s
+    sample = ("per step: 1 of %d layers, %d of %d heads, T=%d verify + commit, greedy accept of "
+              "%d rows over V=%d" % (w["L"], heads, w["H"], w["T"], w["T"], w["V"]))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": HEADLINE, "layers": w["L"], "B": w["B"], "T": w["T"], "H": w["H"],
+                   "dk": w["dk"], "dv": w["dv"], "V": w["V"], "step_sample": sample},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-rows", action="store_true", help="skip the batch and prefill rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+
+    dn.load_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=device)
+        dist = tdist
+
+    w = WORKLOADS[HEADLINE]
+    N, B, T, H, dk, dv = w["L"] * w["B"], w["B"], w["T"], w["H"], w["dk"], w["dv"]
+    sets = make_step_sets(w, device, rank, ROTATE)
+    stream = torch.cuda.Stream(device)
+    clocks = ClockSampler()
+    time.sleep(0.3)
+
+    secs, per, (tw0, tw1) = timed_steps(sets, args.steps, args.warmup, stream, dist)
+    if dist is not None:
+        t = torch.tensor([secs], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        secs = float(t.item())
+    units_per_rank = B * T * w["L"] * args.steps
+    value = units_per_rank * world / secs
+
+    e2e_k = max(3, min(args.steps, 200))
+    e2e_s, h2d, d2h = e2e_steps(w, sets, e2e_k, 3, stream, device)
+    e2e_value = B * T * w["L"] * e2e_k / e2e_s
+
+    rows = {}
+    if not args.no_rows and rank == 0:
+        rows["batch64_step"] = batch_row(device, stream)
+        rows["prefill"] = prefill_row(device, stream)
+    clocks.stop()
+    gpu_index = local
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if cvd and cvd.split(",")[local].strip().isdigit():
+        gpu_index = int(cvd.split(",")[local])
+    clock_info = clocks.summary(tw0, tw1, gpu_index)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    hbm, peak_kind = peaks()
+    vb = verify_bytes(N, T, H, dk, dv, 2)
+    ab = accept_bytes(B, T, w["V"], 2)
+    cb = commit_bytes(w["L"], sets[0]["acc_plan"], H, dk, dv, 2)
+    v_ms, a_ms, c_ms = per
+    achieved = vb / (v_ms / 1e3) / 1e9
+    traffic = ncu_traffic("verify_block_kernel")
+
+    cpu = None
+    if not args.no_cpu and world == 1:
+        d = oracle_inputs(w, H, w["seed"] + 500)
+        s_tot, u_tot, n = 0.0, 0.0, 0
+        while s_tot < 10.0 or n < 2:
+            s, u = oracle_step(w, d)
+            s_tot, u_tot, n = s_tot + s, u_tot + u, n + 1
+        cpu = {"value": u_tot / s_tot, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": "%d repetitions of 1 of 48 layers (48 heads, T=16 verify + commit, "
+                         "greedy accept over V=151936), %.1f s" % (n, s_tot)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; planted argmax, 15 of 16 accepted)",
+        "config": {"workload": HEADLINE, "layers": w["L"], "B": B, "T": T, "H": H, "dk": dk,
+                   "dv": dv, "V": w["V"], "accepted": int(sets[0]["acc_plan"][0]),
+                   "l2": "inputs larger than L2 (%.2f GB per step), %d rotating buffer sets"
+                         % ((vb + ab + cb) / 1e9, ROTATE),
+                   "parallelism": "replicas" if world == 1 else "dp%d (independent requests)" % world},
+        "roofline": {"bound": "hbm", "kernel": "dn_verify_block", "achieved": achieved,
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                     "frac_of_nominal_8tbs": achieved / 8000.0, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": vb, "ms_per_launch": v_ms},
+        "kernels": {
+            "dn_verify_block": {"ms": v_ms, "gbs": achieved, "bytes": vb},
+            "dn_accept_greedy": {"ms": a_ms, "gbs": ab / (a_ms / 1e3) / 1e9, "bytes": ab},
+            "dn_commit": {"ms": c_ms, "gbs": cb / (c_ms / 1e3) / 1e9, "bytes": cb},
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_k},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clock_info,
+        "cpu_baseline": cpu,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -30,7 +30,8 @@ def _gather(x, units):
     out = {}
     for k in KEYS:
         out[k] = np.stack([np64(x[k][n, :, h]) for n, h in units])[:, :, None]
-    out["state"] = np.stack([np64(x["state"][n, h]) for n, h in units])[:, None]
+    if x.get("state") is not None:
+        out["state"] = np.stack([np64(x["state"][n, h]) for n, h in units])[:, None]
     return out
 
 

@@ -32,6 +32,7 @@ SIGNATURES = {
     "dn_prefill_checkpoint": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P]),
     "dn_status_string": (ctypes.c_char_p, [_I]),
+    "dn_accept_greedy_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
 }
 
 

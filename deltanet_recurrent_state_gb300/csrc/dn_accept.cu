@@ -13,6 +13,8 @@
 // the row's chunk keys and writes the target id; the last row of a request then
 // computes the accepted length. Both counters are reset by the CTA that finishes
 // them, so the workspace is ready for the next call. Nothing spins or waits.
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "dn.h"
@@ -187,6 +189,79 @@ extern "C" dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, co
     const AcceptWorkspace ws = accept_ws(workspace, B, T, V);
     const dim3 grid(accept_chunks(V), B * T);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (logit_dt == DN_F16)
+        accept_greedy_kernel<unsigned short><<<grid, kThreads, 0, st>>>(
+            B, T, V, static_cast<const unsigned short *>(logits), draft_ids, target_ids,
+            accepted_len, ws);
+    else
+        accept_greedy_kernel<unsigned int><<<grid, kThreads, 0, st>>>(
+            B, T, V, static_cast<const unsigned int *>(logits), draft_ids, target_ids,
+            accepted_len, ws);
+    return launch_status();
+}
+
+// ---------------------------------------------------------------------------------------
+// dn_accept_greedy_noalloc: the same kernel with its scratch in a fixed device array, for
+// callers that cannot allocate device memory where they verify (see include/dn.h).
+namespace dn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DN_ACCEPT_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch per device. In host code the array's name is
+// only a host-side stand-in; the kernel must be given the address the runtime reports.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+dn_status noalloc_scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (dev >= 0 && dev < kMaxDevices && g_noalloc_addr[dev] != nullptr) {
+        *out = g_noalloc_addr[dev];
+        return DN_OK;
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return DN_ERR_CUDA;
+    }
+    if (dev >= 0 && dev < kMaxDevices) g_noalloc_addr[dev] = p;
+    *out = p;
+    return DN_OK;
+}
+
+}  // namespace
+}  // namespace dn
+
+extern "C" dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logit_dt,
+                                              const void *logits, const int32_t *draft_ids,
+                                              int32_t *target_ids, int32_t *accepted_len,
+                                              dn_stream_t stream) {
+    using namespace dn;
+    if (B < 0 || T < 1 || V < 1 || !dtype_ok(logit_dt)) return DN_ERR_INVALID_ARG;
+    if ((long long)B * T > 65535) return DN_ERR_INVALID_ARG;
+    if (B == 0) return DN_OK;
+    if (!logits || !draft_ids || !target_ids || !accepted_len) return DN_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(draft_ids, 4) || !aligned(target_ids, 4) ||
+        !aligned(accepted_len, 4))
+        return DN_ERR_INVALID_ARG;
+    const size_t need = accept_ws_bytes(B, T, V);
+    if (need > DN_ACCEPT_NOALLOC_SCRATCH_BYTES) return DN_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    const dn_status st_addr = noalloc_scratch_address(&scratch);
+    if (st_addr != DN_OK) return st_addr;
+    const AcceptWorkspace ws = accept_ws(scratch, B, T, V);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // The counters must start at zero; the chunk keys are always written before read.
+    const size_t counters = static_cast<size_t>(
+        static_cast<char *>(scratch) + need - reinterpret_cast<char *>(ws.row_count));
+    if (cudaMemsetAsync(ws.row_count, 0, counters, st) != cudaSuccess) {
+        cudaGetLastError();
+        return DN_ERR_CUDA;
+    }
+    const dim3 grid(accept_chunks(V), B * T);
     if (logit_dt == DN_F16)
         accept_greedy_kernel<unsigned short><<<grid, kThreads, 0, st>>>(
             B, T, V, static_cast<const unsigned short *>(logits), draft_ids, target_ids,

@@ -205,6 +205,38 @@ dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int dk, int dv,
                                 const void *state_in, void *out, void *ckpt,
                                 void *state_out, dn_stream_t stream);
 
+/*
+ * dn_accept_greedy_noalloc -- dn_accept_greedy without a caller-supplied workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory at the point where they verify: a serving engine
+ * that has handed almost all of the GPU's memory to its own page pool at start-up
+ * and refuses further allocations, or plain C code embedded in such a host that
+ * has no access to the host's allocator. Those callers pass the same inputs and
+ * outputs as for dn_accept_greedy, and get the same results, but no workspace.
+ *
+ * The scratch lives in one fixed device array of DN_ACCEPT_NOALLOC_SCRATCH_BYTES
+ * bytes inside libdn.so. Every GPU that loads the library holds that array until
+ * the process exits. The call allocates nothing and frees nothing.
+ *
+ *   - Sizes: calls whose dn_accept_workspace_bytes(B, T, V) exceeds
+ *     DN_ACCEPT_NOALLOC_SCRATCH_BYTES return DN_ERR_INVALID_ARG with nothing
+ *     enqueued (about 1,600 verified positions at V = 151,936). Other arguments are
+ *     checked as for dn_accept_greedy.
+ *   - First call on a device: it looks up the array's device address once per
+ *     device (with that device current) and returns DN_ERR_CUDA if the lookup
+ *     fails. Make that first call before any stream capture on that device.
+ *   - Sharing: all calls on a device share the one array. The call clears the
+ *     counters it needs on `stream` before its kernel runs, so leftovers of an
+ *     earlier call do no harm; but two calls whose work overlaps on the GPU (on
+ *     different streams, or from different threads) race on the array and give
+ *     wrong results. Serialise them.
+ */
+#define DN_ACCEPT_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logit_dt, const void *logits,
+                                   const int32_t *draft_ids, int32_t *target_ids,
+                                   int32_t *accepted_len, dn_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *dn_status_string(dn_status s);
 

@@ -6,10 +6,18 @@
 // Technical Insight; "HyperQwen" README, The numbers behind that).
 //
 // Work decomposition. The dv rows of S evolve independently (row i only needs
-// v_t[i] and the shared k_t, q_t), so a CTA owns ROWS rows of one (state set,
+// v_t[i] and the shared k_t, q_t), so a CTA owns 32 rows of one (state set,
 // head) and keeps that slice in registers, in fp32, for all T tokens. Grid =
-// N * H * (dv / ROWS) CTAs. The kernel is bound by the checkpoint stores (T
-// copies of the state slice), issued as 16-byte streaming stores.
+// N * H * (dv / 32) CTAs. The kernel is bound by the checkpoint stores (T copies
+// of the state slice), issued as 16-byte streaming stores.
+//
+// Two kernels:
+//  * verify_wy_kernel (fp16 state): the chunkwise (WY) form of the block. One
+//    tensor-core contraction per CTA gives S0 k_t and S0 q_t for every t, a 16 x 16
+//    forward substitution per row gives delta_t and o_t, and the per-token loop
+//    only applies the rank-1 checkpoint update. See the derivation below.
+//  * verify_block_kernel (any supported dtype, the fp32 path): the token-by-token
+//    form, two dot products and the update per token on CUDA cores.
 #include <cuda_runtime.h>
 
 #include "dn.h"
@@ -108,6 +116,249 @@ verify_block_kernel(int H, int T, int DV, const IO *__restrict__ q, const IO *__
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// WY (chunkwise) form of one verify block, fp16 state.
+//
+// With Gamma_t = g_0 ... g_t and delta_t = beta_t (v_t - g_t S_{t-1} k_t), the rule
+// S_t = g_t S_{t-1} + delta_t k_t^T unrolls to (gated delta rule, chunkwise form)
+//
+//   S_t     = Gamma_t S0 + sum_{s<=t} (Gamma_t / Gamma_s) delta_s k_s^T
+//   delta_t = beta_t ( v_t - Gamma_t (S0 k_t) - sum_{s<t} L[t][s] delta_s ),
+//             L[t][s] = (Gamma_t / Gamma_s) (k_t . k_s)
+//   o_t     = Gamma_t (S0 q_t) + sum_{s<=t} M[t][s] delta_s,
+//             M[t][s] = (Gamma_t / Gamma_s) (q_t . k_s)
+//
+// Gamma ratios are formed as exp(G_t - G_s) with G the running sum of log g, so
+// they never exceed 1. Per CTA (32 rows of one head):
+//   1. S0 rows, k_t and q_t go to shared memory as fp16 (the contraction operands);
+//   2. mma.sync m16n8k16 (fp16 in, fp32 accumulate): proj[32 x 32] = S0 [K;Q]^T and
+//      gram[32 x 16] = [K;Q] K^T;
+//   3. L, M and Gamma (16 x 16 per head) from gram and the gates;
+//   4. one lane per row solves delta_t by forward substitution;
+//   5. every lane applies S_t = g_t S_{t-1} + delta_t k_t^T to its 16 fp32 state
+//      elements with packed fp32x2 FMAs and streams the fp16 checkpoint;
+//   6. o_t from proj, M and delta.
+// The contraction is a few dozen m16n8k16 MMAs per CTA; its job is to remove the
+// two per-token dot products (two FMAs per state element per token) from the
+// store-bound loop, not throughput, so warp-level MMAs fit it (no TMEM round trip).
+
+__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], const void *p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+__device__ __forceinline__ void ldsm_x2(unsigned (&r)[2], const void *p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(a));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4],
+                                          const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// fp16 tile with CPR 16-byte chunks per row; chunk c of row r lives at c ^ (r & 7),
+// so the 8 row addresses of an ldmatrix hit 8 different bank groups.
+template <int CPR>
+__device__ __forceinline__ int hsw(int r, int c) { return r * CPR + (c ^ (r & 7)); }
+
+__device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
+    uint4 u;
+    __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __float22half2_rn(s[i]);
+    return u;
+}
+
+template <int DK>
+__global__ void __launch_bounds__(256, 5)
+verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
+                 const __half *__restrict__ v, const float *__restrict__ beta,
+                 const float *__restrict__ g, const __half *__restrict__ s_in,
+                 __half *__restrict__ out, __half *__restrict__ ckpt) {
+    constexpr int ROWS = 32, TPR = 8, NT = 256;
+    constexpr int CPR = DK / 8;        // 16-byte chunks per row
+    constexpr int NCH = CPR / TPR;     // chunks per lane
+    constexpr int KS = DK / 16;        // MMA k-steps
+    __shared__ __align__(128) uint4 sS0[ROWS * CPR];
+    __shared__ __align__(128) uint4 sKQ[2 * kMaxT * CPR];  // rows 0..15 k_t, 16..31 q_t
+    __shared__ __align__(16) float sk[kMaxT][DK];           // k_t in fp32 (swz4)
+    __shared__ float proj[ROWS][2 * kMaxT + 1];              // [row][t] S0 k_t, [row][16+t] S0 q_t
+    __shared__ float gram[2 * kMaxT][kMaxT + 1];             // [t][s] k_t.k_s, [16+t][s] q_t.k_s
+    __shared__ float sL[kMaxT][kMaxT], sM[kMaxT][kMaxT];
+    __shared__ float sgam[kMaxT], sG[kMaxT], sbeta[kMaxT], sg[kMaxT];
+    __shared__ float sv[kMaxT][ROWS], sd[kMaxT][ROWS], so[kMaxT][ROWS];
+
+    const int rblocks = DV / ROWS;
+    const int rb = blockIdx.x % rblocks;
+    const int h = (blockIdx.x / rblocks) % H;
+    const size_t n = blockIdx.x / (rblocks * H);
+    const int tid = threadIdx.x, lr = tid / TPR, ln = tid % TPR, row = rb * ROWS + lr;
+    const int warp = tid / 32, lane = tid % 32;
+    const size_t set_elems = (size_t)DV * DK;
+
+    // 1. state chunks c*TPR + ln of this lane's row: fp16 to shared, fp32 to registers
+    float2 s[NCH * 4];
+    {
+        const __half *sp = s_in + (n * H + h) * set_elems + (size_t)row * DK;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int j = c * TPR + ln;
+            const uint4 u = *reinterpret_cast<const uint4 *>(sp + j * 8);
+            sS0[hsw<CPR>(lr, j)] = u;
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
+        }
+    }
+    for (int i = tid; i < kMaxT * CPR; i += NT) {
+        const int t = i / CPR, j = i % CPR;
+        uint4 uk = make_uint4(0u, 0u, 0u, 0u), uq = uk;  // rows past T stay zero
+        if (t < T) {
+            const size_t off = ((n * T + t) * H + h) * DK + (size_t)j * 8;
+            uk = *reinterpret_cast<const uint4 *>(k + off);
+            uq = *reinterpret_cast<const uint4 *>(q + off);
+            float x[8];
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&uk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(h2[e]);
+                x[2 * e] = f.x;
+                x[2 * e + 1] = f.y;
+            }
+            smem_put8(sk[t], j, x);
+        }
+        sKQ[hsw<CPR>(t, j)] = uk;
+        sKQ[hsw<CPR>(kMaxT + t, j)] = uq;
+    }
+    for (int i = tid; i < T * ROWS; i += NT) {
+        const int t = i / ROWS, r = i % ROWS;
+        sv[t][r] = __half2float(v[((n * T + t) * H + h) * DV + rb * ROWS + r]);
+    }
+    if (warp == 0) {
+        // G_t = sum_{r<=t} log g_r: inclusive scan over lanes 0..15
+        float lg = 0.f, gg = 1.f, bb = 0.f;
+        if (lane < T) {
+            gg = g[(n * T + lane) * H + h];
+            bb = beta[(n * T + lane) * H + h];
+            lg = logf(fmaxf(gg, 1e-30f));
+        }
+#pragma unroll
+        for (int off = 1; off < kMaxT; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, lg, off);
+            if (lane >= off) lg += o;
+        }
+        if (lane < kMaxT) {
+            sG[lane] = lg;
+            sgam[lane] = expf(lg);
+            sg[lane] = gg;
+            sbeta[lane] = bb;
+        }
+    }
+    __syncthreads();
+
+    // 2. proj = S0 [K;Q]^T (8 warps, one 16x8 tile each); gram = [K;Q] K^T (warps 0..3)
+    {
+        const int mt = warp >> 2, nt = warp & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            unsigned a[4], b[2];
+            ldsm_x4(a, &sS0[hsw<CPR>(mt * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+            ldsm_x2(b, &sKQ[hsw<CPR>(nt * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+            mma_16816(d, a, b);
+        }
+        const int r0 = mt * 16 + (lane >> 2), c0 = nt * 8 + 2 * (lane & 3);
+        proj[r0][c0] = d[0];
+        proj[r0][c0 + 1] = d[1];
+        proj[r0 + 8][c0] = d[2];
+        proj[r0 + 8][c0 + 1] = d[3];
+        if (warp < 4) {
+            const int gm = warp >> 1, gn = warp & 1;
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                unsigned a[4], b[2];
+                ldsm_x4(a, &sKQ[hsw<CPR>(gm * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+                ldsm_x2(b, &sKQ[hsw<CPR>(gn * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+                mma_16816(e, a, b);
+            }
+            const int g0 = gm * 16 + (lane >> 2), h0 = gn * 8 + 2 * (lane & 3);
+            gram[g0][h0] = e[0];
+            gram[g0][h0 + 1] = e[1];
+            gram[g0 + 8][h0] = e[2];
+            gram[g0 + 8][h0 + 1] = e[3];
+        }
+    }
+    __syncthreads();
+
+    // 3. L (strictly lower) and M (lower incl. diagonal), one entry per thread
+    {
+        const int t = tid >> 4, s2 = tid & 15;
+        const float r = (s2 <= t) ? expf(sG[t] - sG[s2]) : 0.f;
+        sL[t][s2] = (s2 < t) ? r * gram[t][s2] : 0.f;
+        sM[t][s2] = r * gram[kMaxT + t][s2];
+    }
+    __syncthreads();
+
+    // 4. delta_t by forward substitution, one lane per row
+    if (warp == 0) {
+        float dl[kMaxT];
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t) {
+            dl[t] = 0.f;
+            if (t < T) {
+                float acc = 0.f;
+#pragma unroll
+                for (int s2 = 0; s2 < t; ++s2) acc = fmaf(sL[t][s2], dl[s2], acc);
+                dl[t] = sbeta[t] * (sv[t][lane] - sgam[t] * proj[lane][t] - acc);
+                sd[t][lane] = dl[t];
+            }
+        }
+    }
+    __syncthreads();
+
+    // 5. checkpoints S_t = g_t S_{t-1} + delta_t k_t^T
+    __half *dst = ckpt + ((n * T) * H + h) * set_elems + (size_t)row * DK + ln * 8;
+    const size_t tstride = (size_t)H * set_elems;
+    for (int t = 0; t < T; ++t) {
+        const float dt = sd[t][lr], gt = sg[t];
+        const float2 d2 = make_float2(dt, dt), g2 = make_float2(gt, gt);
+        const float4 *k4 = reinterpret_cast<const float4 *>(sk[t]);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int j8 = c * TPR + ln;
+            const float4 ka = k4[swz4(2 * j8)], kb = k4[swz4(2 * j8 + 1)];
+            s[c * 4 + 0] = __ffma2_rn(d2, make_float2(ka.x, ka.y), __fmul2_rn(g2, s[c * 4 + 0]));
+            s[c * 4 + 1] = __ffma2_rn(d2, make_float2(ka.z, ka.w), __fmul2_rn(g2, s[c * 4 + 1]));
+            s[c * 4 + 2] = __ffma2_rn(d2, make_float2(kb.x, kb.y), __fmul2_rn(g2, s[c * 4 + 2]));
+            s[c * 4 + 3] = __ffma2_rn(d2, make_float2(kb.z, kb.w), __fmul2_rn(g2, s[c * 4 + 3]));
+            __stcs(reinterpret_cast<uint4 *>(dst + c * TPR * 8), pack8_half2(&s[c * 4]));
+        }
+        dst += tstride;
+    }
+
+    // 6. outputs
+    for (int i = tid; i < T * ROWS; i += NT) {
+        const int t = i / ROWS, r = i % ROWS;
+        float o = sgam[t] * proj[r][kMaxT + t];
+        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
+        so[t][r] = o;
+    }
+    __syncthreads();
+    for (int i = tid; i < T * ROWS; i += NT) {
+        const int t = i / ROWS, r = i % ROWS;
+        out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(so[t][r]);
+    }
+}
+
 constexpr int kRows = 32;
 constexpr int kTpr = 8;
 
@@ -143,8 +394,14 @@ extern "C" dn_status dn_verify_block(int N, int H, int T, int dk, int dv, dn_dty
     if ((long long)N * H * (dv / kRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (io_dt == DN_F16) {
-        if (dk == 128) launch_verify<128, __half, __half>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
-        else launch_verify<64, __half, __half>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
+        const unsigned blocks = (unsigned)((long long)N * H * (dv / kRows));
+        const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
+        const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
+        __half *oh = static_cast<__half *>(out), *ch = static_cast<__half *>(ckpt);
+        if (dk == 128)
+            verify_wy_kernel<128><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch);
+        else
+            verify_wy_kernel<64><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch);
     } else {
         if (dk == 128) launch_verify<128, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
         else launch_verify<64, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);

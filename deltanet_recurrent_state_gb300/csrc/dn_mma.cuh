@@ -1,0 +1,79 @@
+// Warp-level tensor-core helpers shared by the chunkwise (WY) kernels:
+// ldmatrix loads of fp16 tiles from shared memory, the m16n8k16 fp16 MMA with fp32
+// accumulation, the XOR swizzle of 16-byte chunks that keeps ldmatrix conflict
+// free, and packing of fp32 accumulator fragments into fp16 operand fragments.
+//
+// Fragment layout (per warp, lane L): an m16n8 fp32 accumulator tile holds
+// d0, d1 at row L/4, columns 2(L%4), 2(L%4)+1 and d2, d3 at row L/4 + 8. The fp16
+// A operand of a 16x16 tile holds a0 = rows 0-7 / cols 0-7, a1 = rows 8-15 / cols
+// 0-7, a2 = rows 0-7 / cols 8-15, a3 = rows 8-15 / cols 8-15, each as two fp16
+// at the same (row, column-pair) positions as the accumulator, so two adjacent
+// accumulator tiles repack into one A operand without leaving registers.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_fp16.h>
+
+namespace dn {
+
+__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], const void *p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+__device__ __forceinline__ void ldsm_x2(unsigned (&r)[2], const void *p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(a));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4],
+                                          const unsigned (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// fp16 tile with CPR 16-byte chunks per row; chunk c of row r lives at c ^ (r & 7),
+// so the 8 row addresses of an ldmatrix hit 8 different bank groups.
+template <int CPR>
+__device__ __forceinline__ int hsw(int r, int c) { return r * CPR + (c ^ (r & 7)); }
+
+__device__ __forceinline__ void ldsm_x4_t(unsigned (&r)[4], const void *p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+__device__ __forceinline__ unsigned pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_h2(unsigned u) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&u));
+}
+
+// Two accumulator tiles (columns 0-7 and 8-15 of a 16x16 block) -> one fp16 A operand.
+__device__ __forceinline__ void acc_to_a(unsigned (&a)[4], const float (&d0)[4], const float (&d1)[4]) {
+    a[0] = pack_h2(d0[0], d0[1]);
+    a[1] = pack_h2(d0[2], d0[3]);
+    a[2] = pack_h2(d1[0], d1[1]);
+    a[3] = pack_h2(d1[2], d1[3]);
+}
+
+// cp.async of 16 bytes global -> shared; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(a), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+}  // namespace dn

@@ -4,16 +4,24 @@
 // recurrent state is checkpointed next to the attention context so that a later
 // turn restores it instead of recomputing the prompt).
 //
-// This file holds the sequential form: a CTA owns ROWS rows of one (sequence,
-// head) state in registers and walks the prompt token by token, staging 16
-// tokens of q/k/v/beta/g at a time in shared memory. At every chunk end the
-// carry is rounded to the state dtype and stored, so the carry equals the
-// checkpoint and a restored run continues bit-identically.
+// Two kernels:
+//  * prefill_wy_kernel (fp16 state and io): the chunkwise (WY) form on tensor
+//    cores. A CTA owns one (sequence, head); each warp owns 16 dv-rows of the
+//    state, kept in fp32 MMA accumulator fragments for the whole prompt. Every
+//    16-token sub-chunk costs a handful of m16n8k16 MMAs per warp (derivation at
+//    the kernel); the next 64-token chunk of q/k/v streams in with cp.async while
+//    the current one is processed.
+//  * prefill_seq_kernel (fp32 path): the token-by-token form. A CTA owns ROWS rows
+//    of one (sequence, head) state in registers and walks the prompt, staging 16
+//    tokens of q/k/v/beta/g at a time in shared memory.
+// In both, at every chunk end the carry is rounded to the state dtype and stored,
+// so the carry equals the checkpoint and a restored run continues bit-identically.
 #include <cuda_runtime.h>
 
 #include "dn.h"
 #include "dn_device.cuh"
 #include "dn_internal.h"
+#include "dn_mma.cuh"
 #include "dn_recurrence.cuh"
 
 namespace dn {
@@ -125,6 +133,350 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// Chunkwise (WY) prefill, fp16 state and io.
+//
+// Inside a sub-chunk of 16 tokens starting from state S (dv x dk), with gates
+// accumulated from the sub-chunk start, G_t = sum_{r<=t} log g_r, gam_t = e^{G_t}:
+//   A[t][s]  = beta_t e^{G_t - G_s} (k_t . k_s)          (s < t, else 0)
+//   Tb       = (I + A)^{-1} diag(beta)                    (16 x 16, per head)
+//   Delta    = Tb (V - diag(gam) K S^T)                   (16 x dv)
+//   O        = diag(gam) Q S^T + Mq Delta,  Mq[t][s] = e^{G_t - G_s} (q_t . k_s) (s <= t)
+//   S_next   = gam_15 S + Delta^T diag(e^{G_15 - G}) K
+// which is the token-by-token rule summed over the sub-chunk (the same algebra as
+// the verify block). Four sub-chunks make a 64-token checkpoint chunk.
+//
+// Per chunk (one CTA = one (sequence, head), DV/16 warps):
+//   prep (state independent, all warps): grams K_j K_j^T and Q_j K_j^T by MMA, the
+//     gate scans, A and Mq, and the four 16 x 16 inverses (one thread per column,
+//     forward substitution in fp32);
+//   chain (each warp on its 16 dv-rows, no block barrier inside): per sub-chunk
+//     X = S [K_j;Q_j]^T (MMA, S packed to fp16 from the accumulators), R = V^T -
+//     gam X_K, Delta^T = R Tb^T, O^T = gam X_Q + Delta^T Mq^T, and S += (scaled
+//     Delta)^T K_j on the accumulators;
+//   chunk end: S rounded to fp16 (the carry) and stored as the checkpoint; the O tile
+//     goes out with 16-byte stores.
+// Operands are fp16 with fp32 accumulation; the carry is fp32 inside a chunk.
+
+template <int DK, int DV>
+struct PrefillSmem {
+    static constexpr int C = 64, NSUB = 4;
+    static constexpr int CK = DK / 8, CV = DV / 8;
+    // byte offsets
+    static constexpr size_t kK = 0;                                   // [2][C*CK] uint4
+    static constexpr size_t kQ = kK + 2ull * C * CK * 16;
+    static constexpr size_t kV = kQ + 2ull * C * CK * 16;             // [2][C*CV] uint4
+    static constexpr size_t kO = kV + 2ull * C * CV * 16;             // [C][DV] half
+    static constexpr size_t kGram = kO + (size_t)C * DV * 2;          // [NSUB][2][16][17] float
+    static constexpr size_t kA = kGram + NSUB * 2 * 16 * 17 * 4;      // [NSUB][16][17] float
+    static constexpr size_t kTb = kA + NSUB * 16 * 17 * 4;            // [NSUB][16][24] half
+    static constexpr size_t kMq = kTb + NSUB * 16 * 24 * 2;           // [NSUB][16][24] half
+    static constexpr size_t kG = kMq + NSUB * 16 * 24 * 2;            // [C] float each
+    static constexpr size_t kGam = kG + C * 4;
+    static constexpr size_t kDec = kGam + C * 4;
+    static constexpr size_t kBeta = kDec + C * 4;
+    static constexpr size_t kBytes = kBeta + C * 4;
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(DV * 2)
+prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__restrict__ k,
+                  const __half *__restrict__ v, const float *__restrict__ beta,
+                  const float *__restrict__ g, const __half *s_in, __half *__restrict__ out,
+                  __half *__restrict__ ckpt, __half *s_out) {
+    using L = PrefillSmem<DK, DV>;
+    constexpr int C = L::C, NSUB = L::NSUB, CK = L::CK, CV = L::CV;
+    constexpr int NW = DV / 16, NT = NW * 32;
+    constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
+    constexpr int KS = DK / 16;   // k-steps of the projection
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint4 *sK = reinterpret_cast<uint4 *>(smem + L::kK);
+    uint4 *sQ = reinterpret_cast<uint4 *>(smem + L::kQ);
+    uint4 *sV = reinterpret_cast<uint4 *>(smem + L::kV);
+    __half *sO = reinterpret_cast<__half *>(smem + L::kO);
+    float(*sGram)[2][16][17] = reinterpret_cast<float(*)[2][16][17]>(smem + L::kGram);
+    float(*sA)[16][17] = reinterpret_cast<float(*)[16][17]>(smem + L::kA);
+    __half(*sTb)[16][24] = reinterpret_cast<__half(*)[16][24]>(smem + L::kTb);
+    __half(*sMq)[16][24] = reinterpret_cast<__half(*)[16][24]>(smem + L::kMq);
+    float *sG = reinterpret_cast<float *>(smem + L::kG);
+    float *sgam = reinterpret_cast<float *>(smem + L::kGam);
+    float *sdec = reinterpret_cast<float *>(smem + L::kDec);
+    float *sbeta = reinterpret_cast<float *>(smem + L::kBeta);
+
+    const int h = blockIdx.x % H;
+    const size_t n = blockIdx.x / H;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int i0 = warp * 16;                    // this warp's dv rows
+    const int fr = lane >> 2, fc = 2 * (lane & 3);  // fragment row / column pair
+    const size_t set_elems = (size_t)DV * DK;
+    const size_t state_off = (n * H + h) * set_elems;
+
+    // state accumulators: tile nt covers dk columns 8nt .. 8nt+7 of rows i0 .. i0+15
+    float DS[NTK][4];
+#pragma unroll
+    for (int nt = 0; nt < NTK; ++nt) {
+        float2 lo = make_float2(0.f, 0.f), hi = lo;
+        if (s_in) {
+            lo = __half22float2(*reinterpret_cast<const __half2 *>(
+                s_in + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc));
+            hi = __half22float2(*reinterpret_cast<const __half2 *>(
+                s_in + state_off + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc));
+        }
+        DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
+    }
+
+    const int nchunks = (P + C - 1) / C;
+    const int nfull = P / C;
+    auto issue = [&](int c, int b) {
+        const int p0 = c * C;
+        for (int i = tid; i < C * (2 * CK + CV); i += NT) {
+            int t, ch;
+            const __half *src;
+            uint4 *dst;
+            if (i < C * CK) {
+                t = i / CK; ch = i % CK;
+                src = k + ((n * P + p0 + t) * H + h) * DK + ch * 8;
+                dst = sK + b * C * CK + hsw<CK>(t, ch);
+            } else if (i < 2 * C * CK) {
+                const int i2 = i - C * CK;
+                t = i2 / CK; ch = i2 % CK;
+                src = q + ((n * P + p0 + t) * H + h) * DK + ch * 8;
+                dst = sQ + b * C * CK + hsw<CK>(t, ch);
+            } else {
+                const int i2 = i - 2 * C * CK;
+                t = i2 / CV; ch = i2 % CV;
+                src = v + ((n * P + p0 + t) * H + h) * DV + ch * 8;
+                dst = sV + b * C * CV + hsw<CV>(t, ch);
+            }
+            const bool ok = p0 + t < P;
+            cp_async16(dst, ok ? (const void *)src : (const void *)k, ok ? 16 : 0);
+        }
+    };
+    if (nchunks > 0) issue(0, 0);
+    cp_async_commit();
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int p0 = c * C;
+        const int nc = min(C, P - p0);
+        const int b = c & 1;
+        if (c + 1 < nchunks) issue(c + 1, b ^ 1);
+        cp_async_commit();
+        for (int t = tid; t < C; t += NT) {
+            const bool ok = t < nc;
+            sbeta[t] = ok ? beta[(n * P + p0 + t) * H + h] : 0.f;
+            sG[t] = ok ? logf(fmaxf(g[(n * P + p0 + t) * H + h], 1e-30f)) : 0.f;
+        }
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint4 *cK = sK + b * C * CK, *cQ = sQ + b * C * CK, *cV = sV + b * C * CV;
+
+        // prep 1: grams (tile = (sub-chunk, K or Q rows) x K rows of the sub-chunk)
+        for (int tile = warp; tile < 2 * NSUB; tile += NW) {
+            const int j = tile >> 1, isq = tile & 1;
+            const uint4 *rows = isq ? cQ : cK;
+            float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                unsigned a[4], bb[4];
+                ldsm_x4(a, rows + hsw<CK>(16 * j + (lane & 15), 2 * ks + (lane >> 4)));
+                ldsm_x4(bb, cK + hsw<CK>(16 * j + (lane & 7) + ((lane >> 4) << 3),
+                                         2 * ks + ((lane >> 3) & 1)));
+                const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
+                mma_16816(e0, a, b0);
+                mma_16816(e1, a, b1);
+            }
+            sGram[j][isq][fr][fc] = e0[0]; sGram[j][isq][fr][fc + 1] = e0[1];
+            sGram[j][isq][fr + 8][fc] = e0[2]; sGram[j][isq][fr + 8][fc + 1] = e0[3];
+            sGram[j][isq][fr][8 + fc] = e1[0]; sGram[j][isq][fr][9 + fc] = e1[1];
+            sGram[j][isq][fr + 8][8 + fc] = e1[2]; sGram[j][isq][fr + 8][9 + fc] = e1[3];
+        }
+        // prep 2: gate scans within each 16-token sub-chunk (warps 0, 1: one lane per token)
+        if (warp < 2) {
+            const int t = warp * 32 + lane;
+            float x = sG[t];
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, x, off, 16);
+                if ((lane & 15) >= off) x += o;
+            }
+            const float last = __shfl_sync(0xffffffffu, x, lane | 15);
+            sG[t] = x;
+            sgam[t] = expf(x);
+            sdec[t] = expf(last - x);
+        }
+        __syncthreads();
+        // prep 3: A and Mq
+        for (int e = tid; e < NSUB * 256; e += NT) {
+            const int j = e >> 8, t = (e >> 4) & 15, s2 = e & 15;
+            const float dec = (s2 <= t) ? expf(sG[16 * j + t] - sG[16 * j + s2]) : 0.f;
+            sMq[j][t][s2] = __float2half_rn(dec * sGram[j][1][t][s2]);
+            sA[j][t][s2] = (s2 < t) ? sbeta[16 * j + t] * dec * sGram[j][0][t][s2] : 0.f;
+        }
+        __syncthreads();
+        // prep 4: Tb = (I + A)^{-1} diag(beta), one thread per (sub-chunk, column)
+        if (tid < NSUB * 16) {
+            const int j = tid >> 4, col = tid & 15;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float acc = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < i; ++kk) acc = fmaf(sA[j][i][kk], x[kk], acc);
+                x[i] = (i < col) ? 0.f : (i == col ? 1.f : -acc);
+            }
+            const float bc = sbeta[16 * j + col];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sTb[j][i][col] = __float2half_rn(x[i] * bc);
+        }
+        __syncthreads();
+
+        // chain: each warp on its 16 rows, sub-chunk by sub-chunk
+#pragma unroll 1
+        for (int j = 0; j < NSUB; ++j) {
+            if (16 * j >= nc) break;
+            unsigned aS[KS][4];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) acc_to_a(aS[ks], DS[2 * ks], DS[2 * ks + 1]);
+            float X[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) X[u][0] = X[u][1] = X[u][2] = X[u][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                unsigned bk[4], bq[4];
+                const int r = 16 * j + (lane & 7) + ((lane >> 4) << 3);
+                const int cc = 2 * ks + ((lane >> 3) & 1);
+                ldsm_x4(bk, cK + hsw<CK>(r, cc));
+                ldsm_x4(bq, cQ + hsw<CK>(r, cc));
+                const unsigned k0[2] = {bk[0], bk[1]}, k1[2] = {bk[2], bk[3]};
+                const unsigned q0[2] = {bq[0], bq[1]}, q1[2] = {bq[2], bq[3]};
+                mma_16816(X[0], aS[ks], k0);
+                mma_16816(X[1], aS[ks], k1);
+                mma_16816(X[2], aS[ks], q0);
+                mma_16816(X[3], aS[ks], q1);
+            }
+            unsigned vt[4];
+            ldsm_x4_t(vt, cV + hsw<CV>(16 * j + ((lane >> 4) << 3) + (lane & 7),
+                                       (i0 >> 3) + ((lane >> 3) & 1)));
+            float R[2][4], Dl[2][4], O[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = 16 * j + 8 * nt + fc;
+                const float ga = sgam[t], gb = sgam[t + 1];
+                const float2 lo = unpack_h2(vt[2 * nt]), hi = unpack_h2(vt[2 * nt + 1]);
+                R[nt][0] = lo.x - ga * X[nt][0];
+                R[nt][1] = lo.y - gb * X[nt][1];
+                R[nt][2] = hi.x - ga * X[nt][2];
+                R[nt][3] = hi.y - gb * X[nt][3];
+                O[nt][0] = ga * X[2 + nt][0];
+                O[nt][1] = gb * X[2 + nt][1];
+                O[nt][2] = ga * X[2 + nt][2];
+                O[nt][3] = gb * X[2 + nt][3];
+                Dl[nt][0] = Dl[nt][1] = Dl[nt][2] = Dl[nt][3] = 0.f;
+            }
+            {   // Delta^T = R Tb^T
+                unsigned aR[4], bt[4];
+                acc_to_a(aR, R[0], R[1]);
+                ldsm_x4(bt, &sTb[j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+                const unsigned t0[2] = {bt[0], bt[1]}, t1[2] = {bt[2], bt[3]};
+                mma_16816(Dl[0], aR, t0);
+                mma_16816(Dl[1], aR, t1);
+            }
+            {   // O^T += Delta^T Mq^T
+                unsigned aD[4], bm[4];
+                acc_to_a(aD, Dl[0], Dl[1]);
+                ldsm_x4(bm, &sMq[j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+                const unsigned m0[2] = {bm[0], bm[1]}, m1[2] = {bm[2], bm[3]};
+                mma_16816(O[0], aD, m0);
+                mma_16816(O[1], aD, m1);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = 16 * j + 8 * nt + fc;
+                sO[(size_t)t * DV + i0 + fr] = __float2half_rn(O[nt][0]);
+                sO[(size_t)(t + 1) * DV + i0 + fr] = __float2half_rn(O[nt][1]);
+                sO[(size_t)t * DV + i0 + fr + 8] = __float2half_rn(O[nt][2]);
+                sO[(size_t)(t + 1) * DV + i0 + fr + 8] = __float2half_rn(O[nt][3]);
+            }
+            {   // S = gam_15 S + (Delta^T diag(e^{G_15 - G})) K_j
+                float Dt[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int t = 16 * j + 8 * nt + fc;
+                    const float da = sdec[t], db = sdec[t + 1];
+                    Dt[nt][0] = Dl[nt][0] * da;
+                    Dt[nt][1] = Dl[nt][1] * db;
+                    Dt[nt][2] = Dl[nt][2] * da;
+                    Dt[nt][3] = Dl[nt][3] * db;
+                }
+                unsigned aT[4];
+                acc_to_a(aT, Dt[0], Dt[1]);
+                const float gend = sgam[16 * j + 15];
+#pragma unroll
+                for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) DS[nt][e] *= gend;
+#pragma unroll
+                for (int c2 = 0; c2 < NTK / 2; ++c2) {
+                    unsigned bk[4];
+                    ldsm_x4_t(bk, cK + hsw<CK>(16 * j + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                               2 * c2 + (lane >> 4)));
+                    const unsigned b0[2] = {bk[0], bk[1]}, b1[2] = {bk[2], bk[3]};
+                    mma_16816(DS[2 * c2], aT, b0);
+                    mma_16816(DS[2 * c2 + 1], aT, b1);
+                }
+            }
+        }
+        if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint
+            __half *dst = ckpt + ((n * nfull + c) * H + h) * set_elems;
+#pragma unroll
+            for (int nt = 0; nt < NTK; ++nt) {
+                const __half2 lo = __floats2half2_rn(DS[nt][0], DS[nt][1]);
+                const __half2 hi = __floats2half2_rn(DS[nt][2], DS[nt][3]);
+                *reinterpret_cast<__half2 *>(dst + (size_t)(i0 + fr) * DK + 8 * nt + fc) = lo;
+                *reinterpret_cast<__half2 *>(dst + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc) = hi;
+                const float2 l2 = __half22float2(lo), h2 = __half22float2(hi);
+                DS[nt][0] = l2.x; DS[nt][1] = l2.y; DS[nt][2] = h2.x; DS[nt][3] = h2.y;
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < nc * CV; i += NT) {
+            const int t = i / CV, ch = i % CV;
+            *reinterpret_cast<uint4 *>(out + ((n * P + p0 + t) * H + h) * DV + ch * 8) =
+                reinterpret_cast<const uint4 *>(sO)[t * CV + ch];
+        }
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int nt = 0; nt < NTK; ++nt) {
+        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc) =
+            __floats2half2_rn(DS[nt][0], DS[nt][1]);
+        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc) =
+            __floats2half2_rn(DS[nt][2], DS[nt][3]);
+    }
+}
+
+template <int DK, int DV>
+dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
+                            const float *beta, const float *g, const void *s_in, void *out,
+                            void *ckpt, void *s_out, cudaStream_t st) {
+    constexpr size_t bytes = PrefillSmem<DK, DV>::kBytes;
+    static bool configured = false;  // the attribute is per function and idempotent
+    if (!configured) {
+        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return DN_ERR_CUDA;
+        }
+        configured = true;
+    }
+    prefill_wy_kernel<DK, DV><<<(unsigned)((long long)N * H), DV * 2, bytes, st>>>(
+        H, P, static_cast<const __half *>(q), static_cast<const __half *>(k),
+        static_cast<const __half *>(v), beta, g, static_cast<const __half *>(s_in),
+        static_cast<__half *>(out), static_cast<__half *>(ckpt), static_cast<__half *>(s_out));
+    return DN_OK;
+}
+
 constexpr int kRows = 16;
 constexpr int kTpr = 8;
 
@@ -163,8 +515,12 @@ extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int d
     if ((long long)N * H * (dv / kRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (io_dt == DN_F16) {
-        if (dk == 128) launch_prefill_seq<128, __half, __half>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
-        else launch_prefill_seq<64, __half, __half>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        dn_status r;
+        if (dk == 128 && dv == 128) r = launch_prefill_wy<128, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        else if (dk == 128) r = launch_prefill_wy<128, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        else if (dv == 128) r = launch_prefill_wy<64, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        else r = launch_prefill_wy<64, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        if (r != DN_OK) return r;
     } else {
         if (dk == 128) launch_prefill_seq<128, float, float>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else launch_prefill_seq<64, float, float>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);

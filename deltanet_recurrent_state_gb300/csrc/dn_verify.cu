@@ -23,6 +23,7 @@
 #include "dn.h"
 #include "dn_device.cuh"
 #include "dn_internal.h"
+#include "dn_mma.cuh"
 #include "dn_recurrence.cuh"
 
 namespace dn {
@@ -142,32 +143,6 @@ verify_block_kernel(int H, int T, int DV, const IO *__restrict__ q, const IO *__
 // The contraction is a few dozen m16n8k16 MMAs per CTA; its job is to remove the
 // two per-token dot products (two FMAs per state element per token) from the
 // store-bound loop, not throughput, so warp-level MMAs fit it (no TMEM round trip).
-
-__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], const void *p) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
-}
-
-__device__ __forceinline__ void ldsm_x2(unsigned (&r)[2], const void *p) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-                 : "=r"(r[0]), "=r"(r[1]) : "r"(a));
-}
-
-__device__ __forceinline__ void mma_16816(float (&d)[4], const unsigned (&a)[4],
-                                          const unsigned (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// fp16 tile with CPR 16-byte chunks per row; chunk c of row r lives at c ^ (r & 7),
-// so the 8 row addresses of an ldmatrix hit 8 different bank groups.
-template <int CPR>
-__device__ __forceinline__ int hsw(int r, int c) { return r * CPR + (c ^ (r & 7)); }
 
 __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
     uint4 u;

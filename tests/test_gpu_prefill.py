@@ -41,6 +41,21 @@ def test_fp16_d128(P, with_state, cuda):
     _case(1, P, 4, 128, "f16", 200 + P, with_state, cuda)
 
 
+@pytest.mark.parametrize("P", [0, 1, 15, 16, 17, 63, 65, 200])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_fp16_chunkwise_edges(P, dk, dv, cuda):
+    # the fp16 path (chunkwise tensor-core form): every sub-chunk / chunk boundary case
+    x = inputs.recurrence_inputs(2, P, 3, dk, dv, io="f16", state="f16", seed=400 + P + dk + 2 * dv,
+                                 device="cpu")
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k].to(cuda) for k in KEYS], x["state"].to(cuda))
+    torch.cuda.synchronize()
+    ref = oracle.prefill_checkpoint(*[np64(x[k]) for k in KEYS], np64(x["state"]), chunk=64,
+                                    store="f16", io="f16")
+    assert_close("out", out, ref[0], TOL["f16"])
+    assert_close("ckpt", ckpt, ref[1], TOL["f16"])
+    assert_close("state_out", s_out, ref[2], TOL["f16"])
+
+
 def test_restore_from_checkpoint_is_bit_identical(cuda):
     N, P, H, d = 1, 300, 4, 128
     x = inputs.recurrence_inputs(N, P, H, d, d, seed=301, device=cuda)

@@ -159,15 +159,19 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
 //     goes out with 16-byte stores.
 // Operands are fp16 with fp32 accumulation; the carry is fp32 inside a chunk.
 
-template <int DK, int DV>
+// STAGES: input buffering (2 = the next chunk streams in during the current one).
+// MINB: resident CTAs per SM the register allocation is bounded for. With few
+// (sequence, head) pairs every SM holds at most one CTA and the double buffer hides
+// the loads; with many, two single-buffered CTAs per SM hide each other's phases.
+template <int DK, int DV, int STAGES>
 struct PrefillSmem {
-    static constexpr int C = 64, NSUB = 4;
+    static constexpr int C = 64, NSUB = 4, S = STAGES;
     static constexpr int CK = DK / 8, CV = DV / 8;
     // byte offsets
-    static constexpr size_t kK = 0;                                   // [2][C*CK] uint4
-    static constexpr size_t kQ = kK + 2ull * C * CK * 16;
-    static constexpr size_t kV = kQ + 2ull * C * CK * 16;             // [2][C*CV] uint4
-    static constexpr size_t kO = kV + 2ull * C * CV * 16;             // [C][DV] half
+    static constexpr size_t kK = 0;                                   // [S][C*CK] uint4
+    static constexpr size_t kQ = kK + (size_t)S * C * CK * 16;
+    static constexpr size_t kV = kQ + (size_t)S * C * CK * 16;        // [S][C*CV] uint4
+    static constexpr size_t kO = kV + (size_t)S * C * CV * 16;        // [C][DV] half
     static constexpr size_t kGram = kO + (size_t)C * DV * 2;          // [NSUB][2][16][17] float
     static constexpr size_t kA = kGram + NSUB * 2 * 16 * 17 * 4;      // [NSUB][16][17] float
     static constexpr size_t kTb = kA + NSUB * 16 * 17 * 4;            // [NSUB][16][24] half
@@ -179,13 +183,13 @@ struct PrefillSmem {
     static constexpr size_t kBytes = kBeta + C * 4;
 };
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(DV * 2)
+template <int DK, int DV, int STAGES, int MINB>
+__global__ void __launch_bounds__(DV * 2, MINB)
 prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__restrict__ k,
                   const __half *__restrict__ v, const float *__restrict__ beta,
                   const float *__restrict__ g, const __half *s_in, __half *__restrict__ out,
                   __half *__restrict__ ckpt, __half *s_out) {
-    using L = PrefillSmem<DK, DV>;
+    using L = PrefillSmem<DK, DV, STAGES>;
     constexpr int C = L::C, NSUB = L::NSUB, CK = L::CK, CV = L::CV;
     constexpr int NW = DV / 16, NT = NW * 32;
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
@@ -228,46 +232,59 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
 
     const int nchunks = (P + C - 1) / C;
     const int nfull = P / C;
+    // q/k/v rows of chunk c -> buffer b (rows past P are zero-filled)
     auto issue = [&](int c, int b) {
         const int p0 = c * C;
-        for (int i = tid; i < C * (2 * CK + CV); i += NT) {
-            int t, ch;
-            const __half *src;
-            uint4 *dst;
-            if (i < C * CK) {
-                t = i / CK; ch = i % CK;
-                src = k + ((n * P + p0 + t) * H + h) * DK + ch * 8;
-                dst = sK + b * C * CK + hsw<CK>(t, ch);
-            } else if (i < 2 * C * CK) {
-                const int i2 = i - C * CK;
-                t = i2 / CK; ch = i2 % CK;
-                src = q + ((n * P + p0 + t) * H + h) * DK + ch * 8;
-                dst = sQ + b * C * CK + hsw<CK>(t, ch);
-            } else {
-                const int i2 = i - 2 * C * CK;
-                t = i2 / CV; ch = i2 % CV;
-                src = v + ((n * P + p0 + t) * H + h) * DV + ch * 8;
-                dst = sV + b * C * CV + hsw<CV>(t, ch);
-            }
+        const size_t row0 = (n * P + p0) * H + h;  // (sequence n, token p0, head h)
+        for (int i = tid; i < C * CK; i += NT) {
+            const int t = i / CK, ch = i % CK;
             const bool ok = p0 + t < P;
-            cp_async16(dst, ok ? (const void *)src : (const void *)k, ok ? 16 : 0);
+            const size_t off = (row0 + (size_t)t * H) * DK + ch * 8;
+            cp_async16(sK + b * C * CK + hsw<CK>(t, ch), ok ? (const void *)(k + off) : (const void *)k, ok ? 16 : 0);
+            cp_async16(sQ + b * C * CK + hsw<CK>(t, ch), ok ? (const void *)(q + off) : (const void *)q, ok ? 16 : 0);
+        }
+        for (int i = tid; i < C * CV; i += NT) {
+            const int t = i / CV, ch = i % CV;
+            const bool ok = p0 + t < P;
+            const size_t off = (row0 + (size_t)t * H) * DV + ch * 8;
+            cp_async16(sV + b * C * CV + hsw<CV>(t, ch), ok ? (const void *)(v + off) : (const void *)v, ok ? 16 : 0);
         }
     };
-    if (nchunks > 0) issue(0, 0);
+    // beta and log g of chunk c for token tid (registers, fetched one chunk ahead)
+    auto gates = [&](int c, float &bt, float &lg) {
+        const int t = c * C + tid;
+        bt = 0.f;
+        lg = 0.f;
+        if (tid < C && t < P) {
+            bt = beta[(n * P + t) * H + h];
+            lg = __logf(fmaxf(g[(n * P + t) * H + h], 1e-30f));
+        }
+    };
+    float nbeta = 0.f, nlg = 0.f;
+    if (nchunks > 0) {
+        issue(0, 0);
+        gates(0, nbeta, nlg);
+    }
     cp_async_commit();
 
     for (int c = 0; c < nchunks; ++c) {
         const int p0 = c * C;
         const int nc = min(C, P - p0);
-        const int b = c & 1;
-        if (c + 1 < nchunks) issue(c + 1, b ^ 1);
-        cp_async_commit();
-        for (int t = tid; t < C; t += NT) {
-            const bool ok = t < nc;
-            sbeta[t] = ok ? beta[(n * P + p0 + t) * H + h] : 0.f;
-            sG[t] = ok ? logf(fmaxf(g[(n * P + p0 + t) * H + h], 1e-30f)) : 0.f;
+        const int b = (L::S == 2) ? (c & 1) : 0;
+        if (tid < C) {
+            sbeta[tid] = nbeta;
+            sG[tid] = nlg;
         }
-        cp_async_wait<1>();
+        if (c + 1 < nchunks) gates(c + 1, nbeta, nlg);
+        if (L::S == 2) {
+            if (c + 1 < nchunks) issue(c + 1, b ^ 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            if (c > 0) issue(c, 0);
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
         __syncthreads();
         const uint4 *cK = sK + b * C * CK, *cQ = sQ + b * C * CK, *cV = sV + b * C * CV;
 
@@ -302,14 +319,14 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
             }
             const float last = __shfl_sync(0xffffffffu, x, lane | 15);
             sG[t] = x;
-            sgam[t] = expf(x);
-            sdec[t] = expf(last - x);
+            sgam[t] = __expf(x);
+            sdec[t] = __expf(last - x);
         }
         __syncthreads();
         // prep 3: A and Mq
         for (int e = tid; e < NSUB * 256; e += NT) {
             const int j = e >> 8, t = (e >> 4) & 15, s2 = e & 15;
-            const float dec = (s2 <= t) ? expf(sG[16 * j + t] - sG[16 * j + s2]) : 0.f;
+            const float dec = (s2 <= t) ? __expf(sG[16 * j + t] - sG[16 * j + s2]) : 0.f;
             sMq[j][t][s2] = __float2half_rn(dec * sGram[j][1][t][s2]);
             sA[j][t][s2] = (s2 < t) ? sbeta[16 * j + t] * dec * sGram[j][0][t][s2] : 0.f;
         }
@@ -412,10 +429,13 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 unsigned aT[4];
                 acc_to_a(aT, Dt[0], Dt[1]);
                 const float gend = sgam[16 * j + 15];
+                const float2 g2 = make_float2(gend, gend);
 #pragma unroll
-                for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) DS[nt][e] *= gend;
+                for (int nt = 0; nt < NTK; ++nt) {
+                    const float2 lo = __fmul2_rn(g2, make_float2(DS[nt][0], DS[nt][1]));
+                    const float2 hi = __fmul2_rn(g2, make_float2(DS[nt][2], DS[nt][3]));
+                    DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
+                }
 #pragma unroll
                 for (int c2 = 0; c2 < NTK / 2; ++c2) {
                     unsigned bk[4];
@@ -456,25 +476,45 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
     }
 }
 
-template <int DK, int DV>
-dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
-                            const float *beta, const float *g, const void *s_in, void *out,
-                            void *ckpt, void *s_out, cudaStream_t st) {
-    constexpr size_t bytes = PrefillSmem<DK, DV>::kBytes;
+template <int DK, int DV, int STAGES, int MINB>
+dn_status launch_prefill_wy_cfg(int N, int H, int P, const void *q, const void *k, const void *v,
+                                const float *beta, const float *g, const void *s_in, void *out,
+                                void *ckpt, void *s_out, cudaStream_t st) {
+    constexpr size_t bytes = PrefillSmem<DK, DV, STAGES>::kBytes;
     static bool configured = false;  // the attribute is per function and idempotent
     if (!configured) {
-        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess) {
+        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, STAGES, MINB>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
             cudaGetLastError();
             return DN_ERR_CUDA;
         }
         configured = true;
     }
-    prefill_wy_kernel<DK, DV><<<(unsigned)((long long)N * H), DV * 2, bytes, st>>>(
+    prefill_wy_kernel<DK, DV, STAGES, MINB><<<(unsigned)((long long)N * H), DV * 2, bytes, st>>>(
         H, P, static_cast<const __half *>(q), static_cast<const __half *>(k),
         static_cast<const __half *>(v), beta, g, static_cast<const __half *>(s_in),
         static_cast<__half *>(out), static_cast<__half *>(ckpt), static_cast<__half *>(s_out));
     return DN_OK;
+}
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
+template <int DK, int DV>
+dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
+                            const float *beta, const float *g, const void *s_in, void *out,
+                            void *ckpt, void *s_out, cudaStream_t st) {
+    const long long ctas = (long long)N * H;
+    if (ctas > sm_count())
+        return launch_prefill_wy_cfg<DK, DV, 1, 2>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
+    return launch_prefill_wy_cfg<DK, DV, 2, 1>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
 }
 
 constexpr int kRows = 16;

@@ -3,7 +3,7 @@
     python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3]
     python -m deltanet_recurrent_state_gb300.profile_case accept  [--requests 128]
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
-    python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096]
+    python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1]
 
 Shapes are those of the single-user workload (48 heads, 128 x 128 fp16 state,
 T = 16) with fewer layers, sized so the footprint stays a few hundred MB but
@@ -28,6 +28,7 @@ def main():
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--requests", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--sequences", type=int, default=1)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     a = ap.parse_args()
@@ -50,7 +51,7 @@ def main():
         for _ in range(a.warmup + a.launches):
             dn.dn_accept_greedy(logits, draft, workspace=ws)
     else:
-        x = inputs.recurrence_inputs(1, a.tokens, H, d, d, seed=4, device=dev)
+        x = inputs.recurrence_inputs(a.sequences, a.tokens, H, d, d, seed=4, device=dev)
         for _ in range(a.warmup + a.launches):
             dn.dn_prefill_checkpoint(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
     torch.cuda.synchronize()

@@ -49,6 +49,23 @@ __device__ __forceinline__ void ldsm_x4_t(unsigned (&r)[4], const void *p) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
 }
 
+// Four 8x8 fp16 matrices from fragment registers to shared memory, transposed: lane L
+// gives the address of stored row L % 8 of matrix L / 8, which receives column L % 8
+// of that matrix.
+__device__ __forceinline__ void stsm_x4_t(void *p, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};"
+                 :: "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
+// Named barriers (0 is __syncthreads): sync waits for `count` threads, arrive does not wait.
+__device__ __forceinline__ void bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ unsigned pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const unsigned *>(&h);

@@ -288,7 +288,9 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
         __syncthreads();
         const uint4 *cK = sK + b * C * CK, *cQ = sQ + b * C * CK, *cV = sV + b * C * CV;
 
-        // prep 1: grams (tile = (sub-chunk, K or Q rows) x K rows of the sub-chunk)
+        // prep 1 (all warps): tile = (sub-chunk j, K or Q rows) x K_j^T by MMA, with the
+        // sub-chunk's gate scan done in the same warp; the epilogue applies the decays in
+        // registers: A = beta_t e^{G_t-G_s} k_t.k_s (s < t) and Mq = e^{G_t-G_s} q_t.k_s (s <= t).
         for (int tile = warp; tile < 2 * NSUB; tile += NW) {
             const int j = tile >> 1, isq = tile & 1;
             const uint4 *rows = isq ? cQ : cK;
@@ -303,50 +305,63 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(e0, a, b0);
                 mma_16816(e1, a, b1);
             }
-            sGram[j][isq][fr][fc] = e0[0]; sGram[j][isq][fr][fc + 1] = e0[1];
-            sGram[j][isq][fr + 8][fc] = e0[2]; sGram[j][isq][fr + 8][fc + 1] = e0[3];
-            sGram[j][isq][fr][8 + fc] = e1[0]; sGram[j][isq][fr][9 + fc] = e1[1];
-            sGram[j][isq][fr + 8][8 + fc] = e1[2]; sGram[j][isq][fr + 8][9 + fc] = e1[3];
-        }
-        // prep 2: gate scans within each 16-token sub-chunk (warps 0, 1: one lane per token)
-        if (warp < 2) {
-            const int t = warp * 32 + lane;
-            float x = sG[t];
+            // G_t for t = lane & 15 (inclusive scan of log g within the sub-chunk)
+            float G = sG[16 * j + (lane & 15)];
 #pragma unroll
             for (int off = 1; off < 16; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, x, off, 16);
-                if ((lane & 15) >= off) x += o;
+                const float o = __shfl_up_sync(0xffffffffu, G, off, 16);
+                if ((lane & 15) >= off) G += o;
             }
-            const float last = __shfl_sync(0xffffffffu, x, lane | 15);
-            sG[t] = x;
-            sgam[t] = __expf(x);
-            sdec[t] = __expf(last - x);
+            const float last = __shfl_sync(0xffffffffu, G, 15);
+            if (!isq && lane < 16) {
+                sgam[16 * j + lane] = __expf(G);
+                sdec[16 * j + lane] = __expf(last - G);
+            }
+            const float Gr0 = __shfl_sync(0xffffffffu, G, fr), Gr1 = __shfl_sync(0xffffffffu, G, fr + 8);
+            const float Gc[4] = {__shfl_sync(0xffffffffu, G, fc), __shfl_sync(0xffffffffu, G, fc + 1),
+                                 __shfl_sync(0xffffffffu, G, fc + 8), __shfl_sync(0xffffffffu, G, fc + 9)};
+            const int cs[4] = {fc, fc + 1, fc + 8, fc + 9};
+            const float v0[4] = {e0[0], e0[1], e1[0], e1[1]};   // row fr
+            const float v1[4] = {e0[2], e0[3], e1[2], e1[3]};   // row fr + 8
+            if (!isq) {
+                const float b0r = sbeta[16 * j + fr], b1r = sbeta[16 * j + fr + 8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sA[j][fr][cs[u]] = (cs[u] < fr) ? b0r * __expf(Gr0 - Gc[u]) * v0[u] : 0.f;
+                    sA[j][fr + 8][cs[u]] = (cs[u] < fr + 8) ? b1r * __expf(Gr1 - Gc[u]) * v1[u] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sMq[j][fr][cs[u]] = __float2half_rn((cs[u] <= fr) ? __expf(Gr0 - Gc[u]) * v0[u] : 0.f);
+                    sMq[j][fr + 8][cs[u]] = __float2half_rn((cs[u] <= fr + 8) ? __expf(Gr1 - Gc[u]) * v1[u] : 0.f);
+                }
+            }
         }
-        __syncthreads();
-        // prep 3: A and Mq
-        for (int e = tid; e < NSUB * 256; e += NT) {
-            const int j = e >> 8, t = (e >> 4) & 15, s2 = e & 15;
-            const float dec = (s2 <= t) ? __expf(sG[16 * j + t] - sG[16 * j + s2]) : 0.f;
-            sMq[j][t][s2] = __float2half_rn(dec * sGram[j][1][t][s2]);
-            sA[j][t][s2] = (s2 < t) ? sbeta[16 * j + t] * dec * sGram[j][0][t][s2] : 0.f;
-        }
-        __syncthreads();
-        // prep 4: Tb = (I + A)^{-1} diag(beta), one thread per (sub-chunk, column)
-        if (tid < NSUB * 16) {
+        // prep 2 (warps 0, 1): Tb = (I + A)^{-1} diag(beta), one thread per (sub-chunk,
+        // column). They wait for the gram tiles (barrier 2); the other warps only
+        // announce theirs and go on to the state-dependent projection; everyone meets
+        // at barrier 1 before the first use of Tb.
+        if (warp < 2) {
+            bar_sync(2, NT);
             const int j = tid >> 4, col = tid & 15;
             float x[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float acc = 0.f;
+                float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < i; ++kk) acc = fmaf(sA[j][i][kk], x[kk], acc);
-                x[i] = (i < col) ? 0.f : (i == col ? 1.f : -acc);
+                for (int kk = 0; kk < i; kk += 2) {
+                    acc0 = fmaf(sA[j][i][kk], x[kk], acc0);
+                    if (kk + 1 < i) acc1 = fmaf(sA[j][i][kk + 1], x[kk + 1], acc1);
+                }
+                x[i] = (i < col) ? 0.f : (i == col ? 1.f : -(acc0 + acc1));
             }
             const float bc = sbeta[16 * j + col];
 #pragma unroll
             for (int i = 0; i < 16; ++i) sTb[j][i][col] = __float2half_rn(x[i] * bc);
+        } else {
+            bar_arrive(2, NT);
         }
-        __syncthreads();
 
         // chain: each warp on its 16 rows, sub-chunk by sub-chunk
 #pragma unroll 1
@@ -372,6 +387,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(X[2], aS[ks], q0);
                 mma_16816(X[3], aS[ks], q1);
             }
+            if (j == 0) bar_sync(1, NT);  // Tb, Mq, gam, dec of this chunk are ready
             unsigned vt[4];
             ldsm_x4_t(vt, cV + hsw<CV>(16 * j + ((lane >> 4) << 3) + (lane & 7),
                                        (i0 >> 3) + ((lane >> 3) & 1)));
@@ -407,13 +423,11 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(O[0], aD, m0);
                 mma_16816(O[1], aD, m1);
             }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t = 16 * j + 8 * nt + fc;
-                sO[(size_t)t * DV + i0 + fr] = __float2half_rn(O[nt][0]);
-                sO[(size_t)(t + 1) * DV + i0 + fr] = __float2half_rn(O[nt][1]);
-                sO[(size_t)t * DV + i0 + fr + 8] = __float2half_rn(O[nt][2]);
-                sO[(size_t)(t + 1) * DV + i0 + fr + 8] = __float2half_rn(O[nt][3]);
+            {   // O^T tile -> sO[t][i] (16-byte chunks swizzled by t & 7)
+                const int m = lane >> 3, t = 16 * j + 8 * (m >> 1) + (lane & 7);
+                stsm_x4_t(reinterpret_cast<uint4 *>(sO) + t * CV + (((i0 >> 3) + (m & 1)) ^ (t & 7)),
+                          pack_h2(O[0][0], O[0][1]), pack_h2(O[0][2], O[0][3]),
+                          pack_h2(O[1][0], O[1][1]), pack_h2(O[1][2], O[1][3]));
             }
             {   // S = gam_15 S + (Delta^T diag(e^{G_15 - G})) K_j
                 float Dt[2][4];
@@ -463,7 +477,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
         for (int i = tid; i < nc * CV; i += NT) {
             const int t = i / CV, ch = i % CV;
             *reinterpret_cast<uint4 *>(out + ((n * P + p0 + t) * H + h) * DV + ch * 8) =
-                reinterpret_cast<const uint4 *>(sO)[t * CV + ch];
+                reinterpret_cast<const uint4 *>(sO)[t * CV + (ch ^ (t & 7))];
         }
     }
     cp_async_wait<0>();

@@ -58,6 +58,28 @@ __device__ __forceinline__ void stsm_x4_t(void *p, unsigned r0, unsigned r1, uns
                  :: "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
 }
 
+// Four 8x8 fp16 matrices from fragment registers to shared memory, not transposed.
+__device__ __forceinline__ void stsm_x4(void *p, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
+                 :: "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
+
+// Bulk (TMA engine) copy shared -> global of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void *gmem, const void *smem, unsigned bytes) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gmem), "r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the shared-memory sources of all of this thread's bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Named barriers (0 is __syncthreads): sync waits for `count` threads, arrive does not wait.
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
@@ -87,6 +109,12 @@ __device__ __forceinline__ void acc_to_a(unsigned (&a)[4], const float (&d0)[4],
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
     const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(a), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+// cp.async of 4 bytes global -> shared; src_bytes = 0 writes zero.
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, int src_bytes) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(a), "l"(gmem), "r"(src_bytes)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

@@ -159,39 +159,44 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
 //     goes out with 16-byte stores.
 // Operands are fp16 with fp32 accumulation; the carry is fp32 inside a chunk.
 
-// STAGES: input buffering (2 = the next chunk streams in during the current one).
-// MINB: resident CTAs per SM the register allocation is bounded for. With few
-// (sequence, head) pairs every SM holds at most one CTA and the double buffer hides
-// the loads; with many, two single-buffered CTAs per SM hide each other's phases.
-template <int DK, int DV, int STAGES>
+template <int DK, int DV>
 struct PrefillSmem {
-    static constexpr int C = 64, NSUB = 4, S = STAGES;
+    static constexpr int C = 64, NSUB = 4, NKQV = 3, NPREP = 2;
     static constexpr int CK = DK / 8, CV = DV / 8;
     // byte offsets
-    static constexpr size_t kK = 0;                                   // [S][C*CK] uint4
-    static constexpr size_t kQ = kK + (size_t)S * C * CK * 16;
-    static constexpr size_t kV = kQ + (size_t)S * C * CK * 16;        // [S][C*CV] uint4
-    static constexpr size_t kO = kV + (size_t)S * C * CV * 16;        // [C][DV] half
-    static constexpr size_t kGram = kO + (size_t)C * DV * 2;          // [NSUB][2][16][17] float
-    static constexpr size_t kA = kGram + NSUB * 2 * 16 * 17 * 4;      // [NSUB][16][17] float
-    static constexpr size_t kTb = kA + NSUB * 16 * 17 * 4;            // [NSUB][16][24] half
-    static constexpr size_t kMq = kTb + NSUB * 16 * 24 * 2;           // [NSUB][16][24] half
-    static constexpr size_t kG = kMq + NSUB * 16 * 24 * 2;            // [C] float each
-    static constexpr size_t kGam = kG + C * 4;
-    static constexpr size_t kDec = kGam + C * 4;
-    static constexpr size_t kBeta = kDec + C * 4;
-    static constexpr size_t kBytes = kBeta + C * 4;
+    static constexpr size_t kK = 0;                                      // [3][C*CK] uint4
+    static constexpr size_t kQ = kK + (size_t)NKQV * C * CK * 16;
+    static constexpr size_t kV = kQ + (size_t)NKQV * C * CK * 16;        // [3][C*CV] uint4
+    static constexpr size_t kO = kV + (size_t)NKQV * C * CV * 16;        // [C][DV] half
+    static constexpr size_t kCk = kO + (size_t)C * DV * 2;               // [DV][DK] half
+    static constexpr size_t kTb = kCk + (size_t)DV * DK * 2;             // [2][NSUB][16][24] half
+    static constexpr size_t kMq = kTb + NPREP * NSUB * 16 * 24 * 2;      // [2][NSUB][16][24] half
+    static constexpr size_t kGam = kMq + NPREP * NSUB * 16 * 24 * 2;     // [2][C] float
+    static constexpr size_t kDec = kGam + NPREP * C * 4;                 // [2][C] float
+    static constexpr size_t kA = kDec + NPREP * C * 4;                   // [NSUB][16][17] float
+    static constexpr size_t kGates = kA + NSUB * 16 * 17 * 4;            // [3][2][C] float: beta, g
+    static constexpr size_t kBytes = kGates + (size_t)NKQV * 2 * C * 4;
 };
 
-template <int DK, int DV, int STAGES, int MINB>
-__global__ void __launch_bounds__(DV * 2, MINB)
+// Warp roles. Chain warps (DV/16 of them, 16 dv-rows each) hold the state and run
+// the state-dependent steps of chunk c; four prep warps meanwhile load chunk c+1 and
+// compute its state-independent products. Hand-off per chunk parity p with named
+// barriers over all threads: FULL[p] (prep arrives, chain waits) when chunk c's
+// inputs and products are ready, EMPTY[p] (chain arrives, prep waits) when the
+// chain is done with them. Inputs are triple buffered (chunk c, chunk c+1 and the
+// load of the next one), the prep products double buffered.
+constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6;
+constexpr int kPrepThreads = 128;
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(DV * 2 + kPrepThreads, 1)
 prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__restrict__ k,
                   const __half *__restrict__ v, const float *__restrict__ beta,
                   const float *__restrict__ g, const __half *s_in, __half *__restrict__ out,
                   __half *__restrict__ ckpt, __half *s_out) {
-    using L = PrefillSmem<DK, DV, STAGES>;
+    using L = PrefillSmem<DK, DV>;
     constexpr int C = L::C, NSUB = L::NSUB, CK = L::CK, CV = L::CV;
-    constexpr int NW = DV / 16, NT = NW * 32;
+    constexpr int NW = DV / 16, NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
     extern __shared__ __align__(128) unsigned char smem[];
@@ -199,25 +204,140 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
     uint4 *sQ = reinterpret_cast<uint4 *>(smem + L::kQ);
     uint4 *sV = reinterpret_cast<uint4 *>(smem + L::kV);
     __half *sO = reinterpret_cast<__half *>(smem + L::kO);
-    float(*sGram)[2][16][17] = reinterpret_cast<float(*)[2][16][17]>(smem + L::kGram);
+    uint4 *sCk = reinterpret_cast<uint4 *>(smem + L::kCk);  // 16-byte chunks, swizzled by row & 7
+    __half(*sTb)[NSUB][16][24] = reinterpret_cast<__half(*)[NSUB][16][24]>(smem + L::kTb);
+    __half(*sMq)[NSUB][16][24] = reinterpret_cast<__half(*)[NSUB][16][24]>(smem + L::kMq);
+    float(*sgam)[C] = reinterpret_cast<float(*)[C]>(smem + L::kGam);
+    float(*sdec)[C] = reinterpret_cast<float(*)[C]>(smem + L::kDec);
     float(*sA)[16][17] = reinterpret_cast<float(*)[16][17]>(smem + L::kA);
-    __half(*sTb)[16][24] = reinterpret_cast<__half(*)[16][24]>(smem + L::kTb);
-    __half(*sMq)[16][24] = reinterpret_cast<__half(*)[16][24]>(smem + L::kMq);
-    float *sG = reinterpret_cast<float *>(smem + L::kG);
-    float *sgam = reinterpret_cast<float *>(smem + L::kGam);
-    float *sdec = reinterpret_cast<float *>(smem + L::kDec);
-    float *sbeta = reinterpret_cast<float *>(smem + L::kBeta);
+    float(*sGates)[2][C] = reinterpret_cast<float(*)[2][C]>(smem + L::kGates);  // [buf][beta|g][t]
 
     const int h = blockIdx.x % H;
     const size_t n = blockIdx.x / H;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int i0 = warp * 16;                    // this warp's dv rows
     const int fr = lane >> 2, fc = 2 * (lane & 3);  // fragment row / column pair
     const size_t set_elems = (size_t)DV * DK;
     const size_t state_off = (n * H + h) * set_elems;
+    const int nchunks = (P + C - 1) / C;
+    const int nfull = P / C;
 
-    // state accumulators: tile nt covers dk columns 8nt .. 8nt+7 of rows i0 .. i0+15
-    float DS[NTK][4];
+    if (warp >= NW) {
+        // ============================== prep warps ==============================
+        const int pt = tid - NTC, pw = pt / 32;
+        auto issue = [&](int c) {  // q/k/v rows and gates of chunk c (zero past P)
+            const int p0 = c * C, kb = c % 3;
+            const size_t row0 = (n * P + p0) * H + h;
+            for (int i = pt; i < C * CK; i += NTP) {
+                const int t = i / CK, ch = i % CK;
+                const bool ok = p0 + t < P;
+                const size_t off = (row0 + (size_t)t * H) * DK + ch * 8;
+                cp_async16(sK + kb * C * CK + hsw<CK>(t, ch), ok ? (const void *)(k + off) : (const void *)k, ok ? 16 : 0);
+                cp_async16(sQ + kb * C * CK + hsw<CK>(t, ch), ok ? (const void *)(q + off) : (const void *)q, ok ? 16 : 0);
+            }
+            for (int i = pt; i < C * CV; i += NTP) {
+                const int t = i / CV, ch = i % CV;
+                const bool ok = p0 + t < P;
+                const size_t off = (row0 + (size_t)t * H) * DV + ch * 8;
+                cp_async16(sV + kb * C * CV + hsw<CV>(t, ch), ok ? (const void *)(v + off) : (const void *)v, ok ? 16 : 0);
+            }
+            for (int i = pt; i < 2 * C; i += NTP) {
+                const int which = i / C, t = i % C;
+                const bool ok = p0 + t < P;
+                const float *src = which ? g : beta;
+                cp_async4(&sGates[kb][which][t], ok ? (const void *)(src + row0 + (size_t)t * H) : (const void *)src,
+                          ok ? 4 : 0);
+            }
+        };
+        if (nchunks > 0) issue(0);
+        cp_async_commit();
+        for (int c = 0; c < nchunks; ++c) {
+            const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3;
+            if (c >= 2) bar_sync(kBarEmpty + pb, NTALL);  // chunk c-2 done: products[pb], inputs[(c+1)%3] free
+            if (c + 1 < nchunks) issue(c + 1);
+            cp_async_commit();
+            cp_async_wait<1>();
+            bar_sync(kBarPrep, NTP);
+            const uint4 *cK = sK + kb * C * CK, *cQ = sQ + kb * C * CK;
+            const float *sbeta = sGates[kb][0], *sgr = sGates[kb][1];
+            (void)p0;
+            // grams by MMA, tile = (sub-chunk j, K or Q rows) x K_j^T, with the gate scan of
+            // the sub-chunk in the same warp; the epilogue applies the decays in registers:
+            // A = beta_t e^{G_t-G_s} k_t.k_s (s < t), Mq = e^{G_t-G_s} q_t.k_s (s <= t)
+            for (int tile = pw; tile < 2 * NSUB; tile += NTP / 32) {
+                const int j = tile >> 1, isq = tile & 1;
+                const uint4 *rows = isq ? cQ : cK;
+                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    unsigned a[4], bb[4];
+                    ldsm_x4(a, rows + hsw<CK>(16 * j + (lane & 15), 2 * ks + (lane >> 4)));
+                    ldsm_x4(bb, cK + hsw<CK>(16 * j + (lane & 7) + ((lane >> 4) << 3),
+                                             2 * ks + ((lane >> 3) & 1)));
+                    const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
+                    mma_16816(e0, a, b0);
+                    mma_16816(e1, a, b1);
+                }
+                const int tl = 16 * j + (lane & 15);
+                float G = (tl < nc) ? __logf(fmaxf(sgr[tl], 1e-30f)) : 0.f;  // log g, 0 past the prompt
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, G, off, 16);
+                    if ((lane & 15) >= off) G += o;
+                }
+                const float last = __shfl_sync(0xffffffffu, G, 15);
+                if (!isq && lane < 16) {
+                    sgam[pb][16 * j + lane] = __expf(G);
+                    sdec[pb][16 * j + lane] = __expf(last - G);
+                }
+                const float Gr0 = __shfl_sync(0xffffffffu, G, fr), Gr1 = __shfl_sync(0xffffffffu, G, fr + 8);
+                const float Gc[4] = {__shfl_sync(0xffffffffu, G, fc), __shfl_sync(0xffffffffu, G, fc + 1),
+                                     __shfl_sync(0xffffffffu, G, fc + 8), __shfl_sync(0xffffffffu, G, fc + 9)};
+                const int cs[4] = {fc, fc + 1, fc + 8, fc + 9};
+                const float v0[4] = {e0[0], e0[1], e1[0], e1[1]};  // row fr
+                const float v1[4] = {e0[2], e0[3], e1[2], e1[3]};  // row fr + 8
+                if (!isq) {
+                    const float b0r = sbeta[16 * j + fr], b1r = sbeta[16 * j + fr + 8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        sA[j][fr][cs[u]] = (cs[u] < fr) ? b0r * __expf(Gr0 - Gc[u]) * v0[u] : 0.f;
+                        sA[j][fr + 8][cs[u]] = (cs[u] < fr + 8) ? b1r * __expf(Gr1 - Gc[u]) * v1[u] : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        sMq[pb][j][fr][cs[u]] = __float2half_rn((cs[u] <= fr) ? __expf(Gr0 - Gc[u]) * v0[u] : 0.f);
+                        sMq[pb][j][fr + 8][cs[u]] =
+                            __float2half_rn((cs[u] <= fr + 8) ? __expf(Gr1 - Gc[u]) * v1[u] : 0.f);
+                    }
+                }
+            }
+            bar_sync(kBarPrep, NTP);
+            // Tb = (I + A)^{-1} diag(beta): one thread per (sub-chunk, column), forward
+            // substitution in fp32
+            if (pt < NSUB * 16) {
+                const int j = pt >> 4, col = pt & 15;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < i; ++kk) acc[kk & 3] = fmaf(sA[j][i][kk], x[kk], acc[kk & 3]);
+                    x[i] = (i < col) ? 0.f : (i == col ? 1.f : -((acc[0] + acc[1]) + (acc[2] + acc[3])));
+                }
+                const float bc = sbeta[16 * j + col];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sTb[pb][j][i][col] = __float2half_rn(x[i] * bc);
+            }
+            bar_arrive(kBarFull + pb, NTALL);  // chunk c: inputs and products ready
+            bar_sync(kBarPrep, NTP);           // prep scratch (A) free again
+        }
+        cp_async_wait<0>();
+        return;
+    }
+
+    // ============================== chain warps ==============================
+    const int i0 = warp * 16;  // this warp's dv rows
+    float DS[NTK][4];          // state tile nt: dk columns 8nt .. 8nt+7 of rows i0 .. i0+15
 #pragma unroll
     for (int nt = 0; nt < NTK; ++nt) {
         float2 lo = make_float2(0.f, 0.f), hi = lo;
@@ -230,140 +350,11 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
         DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
     }
 
-    const int nchunks = (P + C - 1) / C;
-    const int nfull = P / C;
-    // q/k/v rows of chunk c -> buffer b (rows past P are zero-filled)
-    auto issue = [&](int c, int b) {
-        const int p0 = c * C;
-        const size_t row0 = (n * P + p0) * H + h;  // (sequence n, token p0, head h)
-        for (int i = tid; i < C * CK; i += NT) {
-            const int t = i / CK, ch = i % CK;
-            const bool ok = p0 + t < P;
-            const size_t off = (row0 + (size_t)t * H) * DK + ch * 8;
-            cp_async16(sK + b * C * CK + hsw<CK>(t, ch), ok ? (const void *)(k + off) : (const void *)k, ok ? 16 : 0);
-            cp_async16(sQ + b * C * CK + hsw<CK>(t, ch), ok ? (const void *)(q + off) : (const void *)q, ok ? 16 : 0);
-        }
-        for (int i = tid; i < C * CV; i += NT) {
-            const int t = i / CV, ch = i % CV;
-            const bool ok = p0 + t < P;
-            const size_t off = (row0 + (size_t)t * H) * DV + ch * 8;
-            cp_async16(sV + b * C * CV + hsw<CV>(t, ch), ok ? (const void *)(v + off) : (const void *)v, ok ? 16 : 0);
-        }
-    };
-    // beta and log g of chunk c for token tid (registers, fetched one chunk ahead)
-    auto gates = [&](int c, float &bt, float &lg) {
-        const int t = c * C + tid;
-        bt = 0.f;
-        lg = 0.f;
-        if (tid < C && t < P) {
-            bt = beta[(n * P + t) * H + h];
-            lg = __logf(fmaxf(g[(n * P + t) * H + h], 1e-30f));
-        }
-    };
-    float nbeta = 0.f, nlg = 0.f;
-    if (nchunks > 0) {
-        issue(0, 0);
-        gates(0, nbeta, nlg);
-    }
-    cp_async_commit();
-
     for (int c = 0; c < nchunks; ++c) {
-        const int p0 = c * C;
-        const int nc = min(C, P - p0);
-        const int b = (L::S == 2) ? (c & 1) : 0;
-        if (tid < C) {
-            sbeta[tid] = nbeta;
-            sG[tid] = nlg;
-        }
-        if (c + 1 < nchunks) gates(c + 1, nbeta, nlg);
-        if (L::S == 2) {
-            if (c + 1 < nchunks) issue(c + 1, b ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            if (c > 0) issue(c, 0);
-            cp_async_commit();
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const uint4 *cK = sK + b * C * CK, *cQ = sQ + b * C * CK, *cV = sV + b * C * CV;
-
-        // prep 1 (all warps): tile = (sub-chunk j, K or Q rows) x K_j^T by MMA, with the
-        // sub-chunk's gate scan done in the same warp; the epilogue applies the decays in
-        // registers: A = beta_t e^{G_t-G_s} k_t.k_s (s < t) and Mq = e^{G_t-G_s} q_t.k_s (s <= t).
-        for (int tile = warp; tile < 2 * NSUB; tile += NW) {
-            const int j = tile >> 1, isq = tile & 1;
-            const uint4 *rows = isq ? cQ : cK;
-            float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                unsigned a[4], bb[4];
-                ldsm_x4(a, rows + hsw<CK>(16 * j + (lane & 15), 2 * ks + (lane >> 4)));
-                ldsm_x4(bb, cK + hsw<CK>(16 * j + (lane & 7) + ((lane >> 4) << 3),
-                                         2 * ks + ((lane >> 3) & 1)));
-                const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
-                mma_16816(e0, a, b0);
-                mma_16816(e1, a, b1);
-            }
-            // G_t for t = lane & 15 (inclusive scan of log g within the sub-chunk)
-            float G = sG[16 * j + (lane & 15)];
-#pragma unroll
-            for (int off = 1; off < 16; off <<= 1) {
-                const float o = __shfl_up_sync(0xffffffffu, G, off, 16);
-                if ((lane & 15) >= off) G += o;
-            }
-            const float last = __shfl_sync(0xffffffffu, G, 15);
-            if (!isq && lane < 16) {
-                sgam[16 * j + lane] = __expf(G);
-                sdec[16 * j + lane] = __expf(last - G);
-            }
-            const float Gr0 = __shfl_sync(0xffffffffu, G, fr), Gr1 = __shfl_sync(0xffffffffu, G, fr + 8);
-            const float Gc[4] = {__shfl_sync(0xffffffffu, G, fc), __shfl_sync(0xffffffffu, G, fc + 1),
-                                 __shfl_sync(0xffffffffu, G, fc + 8), __shfl_sync(0xffffffffu, G, fc + 9)};
-            const int cs[4] = {fc, fc + 1, fc + 8, fc + 9};
-            const float v0[4] = {e0[0], e0[1], e1[0], e1[1]};   // row fr
-            const float v1[4] = {e0[2], e0[3], e1[2], e1[3]};   // row fr + 8
-            if (!isq) {
-                const float b0r = sbeta[16 * j + fr], b1r = sbeta[16 * j + fr + 8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    sA[j][fr][cs[u]] = (cs[u] < fr) ? b0r * __expf(Gr0 - Gc[u]) * v0[u] : 0.f;
-                    sA[j][fr + 8][cs[u]] = (cs[u] < fr + 8) ? b1r * __expf(Gr1 - Gc[u]) * v1[u] : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    sMq[j][fr][cs[u]] = __float2half_rn((cs[u] <= fr) ? __expf(Gr0 - Gc[u]) * v0[u] : 0.f);
-                    sMq[j][fr + 8][cs[u]] = __float2half_rn((cs[u] <= fr + 8) ? __expf(Gr1 - Gc[u]) * v1[u] : 0.f);
-                }
-            }
-        }
-        // prep 2 (warps 0, 1): Tb = (I + A)^{-1} diag(beta), one thread per (sub-chunk,
-        // column). They wait for the gram tiles (barrier 2); the other warps only
-        // announce theirs and go on to the state-dependent projection; everyone meets
-        // at barrier 1 before the first use of Tb.
-        if (warp < 2) {
-            bar_sync(2, NT);
-            const int j = tid >> 4, col = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < i; kk += 2) {
-                    acc0 = fmaf(sA[j][i][kk], x[kk], acc0);
-                    if (kk + 1 < i) acc1 = fmaf(sA[j][i][kk + 1], x[kk + 1], acc1);
-                }
-                x[i] = (i < col) ? 0.f : (i == col ? 1.f : -(acc0 + acc1));
-            }
-            const float bc = sbeta[16 * j + col];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) sTb[j][i][col] = __float2half_rn(x[i] * bc);
-        } else {
-            bar_arrive(2, NT);
-        }
-
-        // chain: each warp on its 16 rows, sub-chunk by sub-chunk
+        const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3;
+        bar_sync(kBarFull + pb, NTALL);
+        const uint4 *cK = sK + kb * C * CK, *cQ = sQ + kb * C * CK, *cV = sV + kb * C * CV;
+        const float *gam = sgam[pb], *dec = sdec[pb];
 #pragma unroll 1
         for (int j = 0; j < NSUB; ++j) {
             if (16 * j >= nc) break;
@@ -374,7 +365,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
 #pragma unroll
             for (int u = 0; u < 4; ++u) X[u][0] = X[u][1] = X[u][2] = X[u][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
+            for (int ks = 0; ks < KS; ++ks) {  // X = S [K_j;Q_j]^T
                 unsigned bk[4], bq[4];
                 const int r = 16 * j + (lane & 7) + ((lane >> 4) << 3);
                 const int cc = 2 * ks + ((lane >> 3) & 1);
@@ -387,15 +378,14 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(X[2], aS[ks], q0);
                 mma_16816(X[3], aS[ks], q1);
             }
-            if (j == 0) bar_sync(1, NT);  // Tb, Mq, gam, dec of this chunk are ready
             unsigned vt[4];
             ldsm_x4_t(vt, cV + hsw<CV>(16 * j + ((lane >> 4) << 3) + (lane & 7),
                                        (i0 >> 3) + ((lane >> 3) & 1)));
             float R[2][4], Dl[2][4], O[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 2; ++nt) {  // R = V^T - gam X_K ; O starts at gam X_Q
                 const int t = 16 * j + 8 * nt + fc;
-                const float ga = sgam[t], gb = sgam[t + 1];
+                const float ga = gam[t], gb = gam[t + 1];
                 const float2 lo = unpack_h2(vt[2 * nt]), hi = unpack_h2(vt[2 * nt + 1]);
                 R[nt][0] = lo.x - ga * X[nt][0];
                 R[nt][1] = lo.y - gb * X[nt][1];
@@ -410,7 +400,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
             {   // Delta^T = R Tb^T
                 unsigned aR[4], bt[4];
                 acc_to_a(aR, R[0], R[1]);
-                ldsm_x4(bt, &sTb[j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+                ldsm_x4(bt, &sTb[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
                 const unsigned t0[2] = {bt[0], bt[1]}, t1[2] = {bt[2], bt[3]};
                 mma_16816(Dl[0], aR, t0);
                 mma_16816(Dl[1], aR, t1);
@@ -418,7 +408,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
             {   // O^T += Delta^T Mq^T
                 unsigned aD[4], bm[4];
                 acc_to_a(aD, Dl[0], Dl[1]);
-                ldsm_x4(bm, &sMq[j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+                ldsm_x4(bm, &sMq[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
                 const unsigned m0[2] = {bm[0], bm[1]}, m1[2] = {bm[2], bm[3]};
                 mma_16816(O[0], aD, m0);
                 mma_16816(O[1], aD, m1);
@@ -434,7 +424,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int t = 16 * j + 8 * nt + fc;
-                    const float da = sdec[t], db = sdec[t + 1];
+                    const float da = dec[t], db = dec[t + 1];
                     Dt[nt][0] = Dl[nt][0] * da;
                     Dt[nt][1] = Dl[nt][1] * db;
                     Dt[nt][2] = Dl[nt][2] * da;
@@ -442,7 +432,7 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 }
                 unsigned aT[4];
                 acc_to_a(aT, Dt[0], Dt[1]);
-                const float gend = sgam[16 * j + 15];
+                const float gend = gam[16 * j + 15];
                 const float2 g2 = make_float2(gend, gend);
 #pragma unroll
                 for (int nt = 0; nt < NTK; ++nt) {
@@ -461,26 +451,40 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 }
             }
         }
-        if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint
-            __half *dst = ckpt + ((n * nfull + c) * H + h) * set_elems;
+        if (c + 2 < nchunks) bar_arrive(kBarEmpty + pb, NTALL);  // inputs / products of chunk c consumed
+        if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged in shared
 #pragma unroll
-            for (int nt = 0; nt < NTK; ++nt) {
-                const __half2 lo = __floats2half2_rn(DS[nt][0], DS[nt][1]);
-                const __half2 hi = __floats2half2_rn(DS[nt][2], DS[nt][3]);
-                *reinterpret_cast<__half2 *>(dst + (size_t)(i0 + fr) * DK + 8 * nt + fc) = lo;
-                *reinterpret_cast<__half2 *>(dst + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc) = hi;
-                const float2 l2 = __half22float2(lo), h2 = __half22float2(hi);
-                DS[nt][0] = l2.x; DS[nt][1] = l2.y; DS[nt][2] = h2.x; DS[nt][3] = h2.y;
+            for (int c2 = 0; c2 < NTK / 2; ++c2) {
+                unsigned r[4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const __half2 lo = __floats2half2_rn(DS[2 * c2 + u][0], DS[2 * c2 + u][1]);
+                    const __half2 hi = __floats2half2_rn(DS[2 * c2 + u][2], DS[2 * c2 + u][3]);
+                    r[2 * u] = *reinterpret_cast<const unsigned *>(&lo);
+                    r[2 * u + 1] = *reinterpret_cast<const unsigned *>(&hi);
+                    const float2 l2 = __half22float2(lo), h2 = __half22float2(hi);
+                    DS[2 * c2 + u][0] = l2.x; DS[2 * c2 + u][1] = l2.y;
+                    DS[2 * c2 + u][2] = h2.x; DS[2 * c2 + u][3] = h2.y;
+                }
+                // matrices: rows 0-7 / 8-15 of dk columns 16c2.., then of 16c2+8..
+                const int m = lane >> 3, row = i0 + (m & 1) * 8 + (lane & 7);
+                stsm_x4(sCk + row * CK + ((2 * c2 + (m >> 1)) ^ (row & 7)), r[0], r[1], r[2], r[3]);
             }
         }
-        __syncthreads();
-        for (int i = tid; i < nc * CV; i += NT) {
+        bar_sync(kBarChain, NTC);  // the O tile (and the checkpoint tile) are complete
+        for (int i = tid; i < nc * CV; i += NTC) {
             const int t = i / CV, ch = i % CV;
             *reinterpret_cast<uint4 *>(out + ((n * P + p0 + t) * H + h) * DV + ch * 8) =
                 reinterpret_cast<const uint4 *>(sO)[t * CV + (ch ^ (t & 7))];
         }
+        if (nc == C) {
+            uint4 *dst = reinterpret_cast<uint4 *>(ckpt + ((n * nfull + c) * H + h) * set_elems);
+            for (int i = tid; i < DV * CK; i += NTC) {
+                const int row = i / CK, ch = i % CK;
+                __stcs(dst + i, sCk[row * CK + (ch ^ (row & 7))]);
+            }
+        }
     }
-    cp_async_wait<0>();
 #pragma unroll
     for (int nt = 0; nt < NTK; ++nt) {
         *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc) =
@@ -490,45 +494,25 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
     }
 }
 
-template <int DK, int DV, int STAGES, int MINB>
-dn_status launch_prefill_wy_cfg(int N, int H, int P, const void *q, const void *k, const void *v,
-                                const float *beta, const float *g, const void *s_in, void *out,
-                                void *ckpt, void *s_out, cudaStream_t st) {
-    constexpr size_t bytes = PrefillSmem<DK, DV, STAGES>::kBytes;
+template <int DK, int DV>
+dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
+                            const float *beta, const float *g, const void *s_in, void *out,
+                            void *ckpt, void *s_out, cudaStream_t st) {
+    constexpr size_t bytes = PrefillSmem<DK, DV>::kBytes;
     static bool configured = false;  // the attribute is per function and idempotent
     if (!configured) {
-        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, STAGES, MINB>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)bytes) != cudaSuccess) {
             cudaGetLastError();
             return DN_ERR_CUDA;
         }
         configured = true;
     }
-    prefill_wy_kernel<DK, DV, STAGES, MINB><<<(unsigned)((long long)N * H), DV * 2, bytes, st>>>(
+    prefill_wy_kernel<DK, DV><<<(unsigned)((long long)N * H), DV * 2 + kPrepThreads, bytes, st>>>(
         H, P, static_cast<const __half *>(q), static_cast<const __half *>(k),
         static_cast<const __half *>(v), beta, g, static_cast<const __half *>(s_in),
         static_cast<__half *>(out), static_cast<__half *>(ckpt), static_cast<__half *>(s_out));
     return DN_OK;
-}
-
-int sm_count() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return sms;
-}
-
-template <int DK, int DV>
-dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
-                            const float *beta, const float *g, const void *s_in, void *out,
-                            void *ckpt, void *s_out, cudaStream_t st) {
-    const long long ctas = (long long)N * H;
-    if (ctas > sm_count())
-        return launch_prefill_wy_cfg<DK, DV, 1, 2>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
-    return launch_prefill_wy_cfg<DK, DV, 2, 1>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
 }
 
 constexpr int kRows = 16;

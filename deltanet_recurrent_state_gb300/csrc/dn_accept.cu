@@ -112,14 +112,25 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
     const bool vec_ok = ((size_t)V * sizeof(E)) % 16 == 0;
     int done = c0;
     if (vec_ok) {
+        // all of this thread's 16-byte loads are issued before any is used
+        constexpr int kPer = kChunk / (VEC * kThreads);
         const int nvec = (c1 - c0) / VEC;
         const uint4 *vp = reinterpret_cast<const uint4 *>(rp + c0);
-        for (int i = threadIdx.x; i < nvec; i += kThreads) {
-            const uint4 u = __ldcs(vp + i);
-            const E *e = reinterpret_cast<const E *>(&u);
-            const int base = c0 + i * VEC;
+        uint4 u[kPer];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) best = umax64(best, pack_key(order_key(e[j]), base + j));
+        for (int r = 0; r < kPer; ++r) {
+            const int i = threadIdx.x + r * kThreads;
+            if (i < nvec) u[r] = __ldcs(vp + i);
+        }
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const int i = threadIdx.x + r * kThreads;
+            if (i < nvec) {
+                const E *e = reinterpret_cast<const E *>(&u[r]);
+                const int base = c0 + i * VEC;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) best = umax64(best, pack_key(order_key(e[j]), base + j));
+            }
         }
         done = c0 + nvec * VEC;
     }
@@ -142,25 +153,31 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
     for (int i = threadIdx.x; i < chunks; i += kThreads)
         k = umax64(k, __ldcg(&ws.keys[(size_t)row * chunks + i]));
     k = block_max(k, red);
-    if (threadIdx.x == 0) {
-        const int tgt = (int)(0xffffffffu - (unsigned int)(k & 0xffffffffull));
-        target[row] = tgt;
-        ws.row_count[row] = 0u;
-        __threadfence();
+    if (threadIdx.x < 32) {  // warp 0 finishes the row, and the request when it is the last row
         const int b = row / T;
-        const unsigned int prev = atomicAdd(&ws.req_count[b], 1u);
+        unsigned int prev = 0;
+        if (threadIdx.x == 0) {
+            target[row] = (int)(0xffffffffu - (unsigned int)(k & 0xffffffffull));
+            ws.row_count[row] = 0u;
+            __threadfence();
+            prev = atomicAdd(&ws.req_count[b], 1u);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == (unsigned int)T - 1) {
-            // Last row of request b: every target of b is written and visible.
+            // Last row of request b: every target of b is written and visible. The
+            // accepted length is the first mismatch, found 32 positions per step.
             __threadfence();
             int a = T;
-            for (int t = 0; t < T; ++t) {
-                if (__ldcg(&draft[b * T + t]) != __ldcg(&target[b * T + t])) {
-                    a = t;
-                    break;
-                }
+            for (int t0 = 0; t0 < T && a == T; t0 += 32) {
+                const int t = t0 + (int)threadIdx.x;
+                const bool miss = t < T && __ldcg(&draft[b * T + t]) != __ldcg(&target[b * T + t]);
+                const unsigned m = __ballot_sync(0xffffffffu, miss);
+                if (m) a = t0 + __ffs(m) - 1;
             }
-            accepted[b] = a;
-            ws.req_count[b] = 0u;
+            if (threadIdx.x == 0) {
+                accepted[b] = a;
+                ws.req_count[b] = 0u;
+            }
         }
     }
 }

@@ -18,8 +18,8 @@ namespace dn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
-constexpr size_t kPiece = (size_t)kThreads * kUnroll * 16;  // 16 KiB per CTA
+constexpr int kUnroll = 8;
+constexpr size_t kPiece = (size_t)kThreads * kUnroll * 16;  // 32 KiB per CTA
 
 __global__ void __launch_bounds__(kThreads)
 commit_kernel(int B, int T, size_t set_bytes, const uint4 *__restrict__ ckpt,

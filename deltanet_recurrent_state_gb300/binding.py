@@ -33,6 +33,7 @@ SIGNATURES = {
                                    _P, _P, _P]),
     "dn_status_string": (ctypes.c_char_p, [_I]),
     "dn_accept_greedy_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "dn_prefill_wait_timeouts": (ctypes.c_uint, []),
 }
 
 
@@ -188,6 +189,10 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
         _ptr(state_out), _stream(stream))
     _check("dn_prefill_checkpoint", st)
     return out, ckpt, state_out
+
+
+def dn_prefill_wait_timeouts():
+    return int(load_library().dn_prefill_wait_timeouts())
 
 
 def dn_status_string(status):

@@ -65,19 +65,55 @@ __device__ __forceinline__ void stsm_x4(void *p, unsigned r0, unsigned r1, unsig
                  :: "r"(a), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
 }
 
-// Bulk (TMA engine) copy shared -> global of `bytes` (multiple of 16, both addresses
-// 16-byte aligned), tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void *gmem, const void *smem, unsigned bytes) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(gmem), "r"(a), "r"(bytes) : "memory");
+// ---- mbarrier and tensor-map (TMA) copies -------------------------------------------
+
+__device__ __forceinline__ void mbar_init(unsigned long long *mb, unsigned count) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(a), "r"(count) : "memory");
+}
+// One arrival that also announces `bytes` of copies still to land in this phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *mb, unsigned bytes) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(a), "r"(bytes) : "memory");
+}
+// Bounded wait for the phase with the given parity; false if it did not complete within
+// `tries` polls (the caller reports it instead of hanging).
+__device__ __forceinline__ bool mbar_wait(unsigned long long *mb, unsigned parity, int tries) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
+    for (int it = 0; it < tries; ++it) {
+        unsigned ok;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// Box of a 4-d tensor map -> shared memory, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void tma_load_4d(void *smem, const void *tmap, int c0, int c1, int c2, int c3,
+                                            unsigned long long *mb) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem);
+    const unsigned m = (unsigned)__cvta_generic_to_shared(mb);
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 :: "r"(d), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(m) : "memory");
+}
+// Shared memory -> box of a 4-d / 3-d tensor map (elements outside the tensor are skipped).
+__device__ __forceinline__ void tma_store_4d(const void *tmap, int c0, int c1, int c2, int c3, const void *smem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                 :: "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(s) : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2, const void *smem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 :: "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(s) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared-memory sources of all of this thread's bulk groups have been read.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until all of this thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy.
+// Order this thread's generic-proxy shared-memory accesses before later async-proxy ones.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Named barriers (0 is __syncthreads): sync waits for `count` threads, arrive does not wait.

@@ -16,6 +16,10 @@
 //    tokens of q/k/v/beta/g at a time in shared memory.
 // In both, at every chunk end the carry is rounded to the state dtype and stored,
 // so the carry equals the checkpoint and a restored run continues bit-identically.
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "dn.h"
@@ -159,24 +163,35 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
 //     goes out with 16-byte stores.
 // Operands are fp16 with fp32 accumulation; the carry is fp32 inside a chunk.
 
+// Shared-memory tiles. q/k/v, O and the checkpoint move with the tensor-map (TMA) engine
+// in 64-column boxes of 128-byte rows, swizzled by the engine: 16-byte chunk c of row r
+// of a box sits at chunk c ^ (r & 7). Every box starts on a 1024-byte boundary.
 template <int DK, int DV>
 struct PrefillSmem {
     static constexpr int C = 64, NSUB = 4, NKQV = 3, NPREP = 2;
-    static constexpr int CK = DK / 8, CV = DV / 8;
+    static constexpr int KH = DK / 64, VH = DV / 64;    // 64-column boxes per row
+    static constexpr size_t kBox = (size_t)C * 128;      // one 64 x 64 fp16 box
     // byte offsets
-    static constexpr size_t kK = 0;                                      // [3][C*CK] uint4
-    static constexpr size_t kQ = kK + (size_t)NKQV * C * CK * 16;
-    static constexpr size_t kV = kQ + (size_t)NKQV * C * CK * 16;        // [3][C*CV] uint4
-    static constexpr size_t kO = kV + (size_t)NKQV * C * CV * 16;        // [C][DV] half
-    static constexpr size_t kCk = kO + (size_t)C * DV * 2;               // [DV][DK] half
-    static constexpr size_t kTb = kCk + (size_t)DV * DK * 2;             // [2][NSUB][16][24] half
+    static constexpr size_t kK = 0;                                       // [3][KH] boxes
+    static constexpr size_t kQ = kK + (size_t)NKQV * KH * kBox;
+    static constexpr size_t kV = kQ + (size_t)NKQV * KH * kBox;          // [3][VH] boxes
+    static constexpr size_t kO = kV + (size_t)NKQV * VH * kBox;          // [2][VH] boxes
+    static constexpr size_t kCk = kO + (size_t)2 * VH * kBox;            // [KH] boxes of DV rows
+    static constexpr size_t kTb = kCk + (size_t)KH * DV * 128;           // [2][NSUB][16][24] half
     static constexpr size_t kMq = kTb + NPREP * NSUB * 16 * 24 * 2;      // [2][NSUB][16][24] half
     static constexpr size_t kGam = kMq + NPREP * NSUB * 16 * 24 * 2;     // [2][C] float
     static constexpr size_t kDec = kGam + NPREP * C * 4;                 // [2][C] float
     static constexpr size_t kA = kDec + NPREP * C * 4;                   // [NSUB][16][17] float
     static constexpr size_t kGates = kA + NSUB * 16 * 17 * 4;            // [3][2][C] float: beta, g
-    static constexpr size_t kBytes = kGates + (size_t)NKQV * 2 * C * 4;
+    static constexpr size_t kMbar = kGates + (size_t)NKQV * 2 * C * 4;   // [3] mbarrier
+    static constexpr size_t kBytes = kMbar + NKQV * 8;
 };
+
+// 16-byte chunk `ch` (of D/8) of row `r` in a run of 64-column swizzled boxes with
+// `rows` rows each.
+__device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
+    return (ch >> 3) * rows * 8 + r * 8 + ((ch & 7) ^ (r & 7));
+}
 
 // Warp roles. Chain warps (DV/16 of them, 16 dv-rows each) hold the state and run
 // the state-dependent steps of chunk c; four prep warps meanwhile load chunk c+1 and
@@ -187,59 +202,72 @@ struct PrefillSmem {
 // load of the next one), the prep products double buffered.
 constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6;
 constexpr int kPrepThreads = 128;
+constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
+
+// Count of prefill input waits that ran out (read by dn_prefill_wait_timeouts).
+__device__ unsigned int g_prefill_wait_timeouts;
+
+struct PrefillMaps {
+    CUtensorMap q, k, v, o, ck;
+};
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(DV * 2 + kPrepThreads, 1)
-prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__restrict__ k,
-                  const __half *__restrict__ v, const float *__restrict__ beta,
-                  const float *__restrict__ g, const __half *s_in, __half *__restrict__ out,
-                  __half *__restrict__ ckpt, __half *s_out) {
+prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
+                  const float *__restrict__ beta, const float *__restrict__ g,
+                  const __half *s_in, __half *s_out) {
     using L = PrefillSmem<DK, DV>;
-    constexpr int C = L::C, NSUB = L::NSUB, CK = L::CK, CV = L::CV;
+    constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
     constexpr int NW = DV / 16, NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
-    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int BOXU = C * 8;   // uint4 per 64 x 64 box
+    extern __shared__ __align__(1024) unsigned char smem[];
     uint4 *sK = reinterpret_cast<uint4 *>(smem + L::kK);
     uint4 *sQ = reinterpret_cast<uint4 *>(smem + L::kQ);
     uint4 *sV = reinterpret_cast<uint4 *>(smem + L::kV);
-    __half *sO = reinterpret_cast<__half *>(smem + L::kO);
-    uint4 *sCk = reinterpret_cast<uint4 *>(smem + L::kCk);  // 16-byte chunks, swizzled by row & 7
+    uint4 *sO = reinterpret_cast<uint4 *>(smem + L::kO);
+    uint4 *sCk = reinterpret_cast<uint4 *>(smem + L::kCk);
     __half(*sTb)[NSUB][16][24] = reinterpret_cast<__half(*)[NSUB][16][24]>(smem + L::kTb);
     __half(*sMq)[NSUB][16][24] = reinterpret_cast<__half(*)[NSUB][16][24]>(smem + L::kMq);
     float(*sgam)[C] = reinterpret_cast<float(*)[C]>(smem + L::kGam);
     float(*sdec)[C] = reinterpret_cast<float(*)[C]>(smem + L::kDec);
     float(*sA)[16][17] = reinterpret_cast<float(*)[16][17]>(smem + L::kA);
     float(*sGates)[2][C] = reinterpret_cast<float(*)[2][C]>(smem + L::kGates);  // [buf][beta|g][t]
+    unsigned long long *mbar = reinterpret_cast<unsigned long long *>(smem + L::kMbar);
 
     const int h = blockIdx.x % H;
-    const size_t n = blockIdx.x / H;
+    const int n = blockIdx.x / H;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int fr = lane >> 2, fc = 2 * (lane & 3);  // fragment row / column pair
     const size_t set_elems = (size_t)DV * DK;
-    const size_t state_off = (n * H + h) * set_elems;
+    const size_t state_off = ((size_t)n * H + h) * set_elems;
     const int nchunks = (P + C - 1) / C;
     const int nfull = P / C;
+
+    if (tid == NTC) {
+        for (int b = 0; b < 3; ++b) mbar_init(&mbar[b], 1);
+        fence_proxy_async();
+    }
+    __syncthreads();
 
     if (warp >= NW) {
         // ============================== prep warps ==============================
         const int pt = tid - NTC, pw = pt / 32;
-        auto issue = [&](int c) {  // q/k/v rows and gates of chunk c (zero past P)
+        // chunk c: q/k/v boxes by the TMA engine on mbar[c % 3] (rows past the prompt
+        // arrive as zeros), beta and g by 4-byte cp.async (zeros past the prompt)
+        auto issue = [&](int c) {
             const int p0 = c * C, kb = c % 3;
-            const size_t row0 = (n * P + p0) * H + h;
-            for (int i = pt; i < C * CK; i += NTP) {
-                const int t = i / CK, ch = i % CK;
-                const bool ok = p0 + t < P;
-                const size_t off = (row0 + (size_t)t * H) * DK + ch * 8;
-                cp_async16(sK + kb * C * CK + hsw<CK>(t, ch), ok ? (const void *)(k + off) : (const void *)k, ok ? 16 : 0);
-                cp_async16(sQ + kb * C * CK + hsw<CK>(t, ch), ok ? (const void *)(q + off) : (const void *)q, ok ? 16 : 0);
+            if (pt == 0) {
+                mbar_arrive_expect_tx(&mbar[kb], (unsigned)((2 * KH + VH) * L::kBox));
+                for (int x = 0; x < KH; ++x) {
+                    tma_load_4d(sK + (kb * KH + x) * BOXU, &maps.k, 64 * x, h, p0, n, &mbar[kb]);
+                    tma_load_4d(sQ + (kb * KH + x) * BOXU, &maps.q, 64 * x, h, p0, n, &mbar[kb]);
+                }
+                for (int x = 0; x < VH; ++x)
+                    tma_load_4d(sV + (kb * VH + x) * BOXU, &maps.v, 64 * x, h, p0, n, &mbar[kb]);
             }
-            for (int i = pt; i < C * CV; i += NTP) {
-                const int t = i / CV, ch = i % CV;
-                const bool ok = p0 + t < P;
-                const size_t off = (row0 + (size_t)t * H) * DV + ch * 8;
-                cp_async16(sV + kb * C * CV + hsw<CV>(t, ch), ok ? (const void *)(v + off) : (const void *)v, ok ? 16 : 0);
-            }
+            const size_t row0 = ((size_t)n * P + p0) * H + h;
             for (int i = pt; i < 2 * C; i += NTP) {
                 const int which = i / C, t = i % C;
                 const bool ok = p0 + t < P;
@@ -256,8 +284,10 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
             if (c + 1 < nchunks) issue(c + 1);
             cp_async_commit();
             cp_async_wait<1>();
+            if (!mbar_wait(&mbar[kb], (unsigned)((c / 3) & 1), kWaitTries) && lane == 0)
+                atomicAdd(&g_prefill_wait_timeouts, 1u);
             bar_sync(kBarPrep, NTP);
-            const uint4 *cK = sK + kb * C * CK, *cQ = sQ + kb * C * CK;
+            const uint4 *cK = sK + kb * KH * BOXU, *cQ = sQ + kb * KH * BOXU;
             const float *sbeta = sGates[kb][0], *sgr = sGates[kb][1];
             (void)p0;
             // grams by MMA, tile = (sub-chunk j, K or Q rows) x K_j^T, with the gate scan of
@@ -270,9 +300,9 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     unsigned a[4], bb[4];
-                    ldsm_x4(a, rows + hsw<CK>(16 * j + (lane & 15), 2 * ks + (lane >> 4)));
-                    ldsm_x4(bb, cK + hsw<CK>(16 * j + (lane & 7) + ((lane >> 4) << 3),
-                                             2 * ks + ((lane >> 3) & 1)));
+                    ldsm_x4(a, rows + box_chunk(C, 16 * j + (lane & 15), 2 * ks + (lane >> 4)));
+                    ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
+                                               2 * ks + ((lane >> 3) & 1)));
                     const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
                     mma_16816(e0, a, b0);
                     mma_16816(e1, a, b1);
@@ -351,9 +381,13 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
     }
 
     for (int c = 0; c < nchunks; ++c) {
-        const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3;
+        const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3, ob = c & 1;
         bar_sync(kBarFull + pb, NTALL);
-        const uint4 *cK = sK + kb * C * CK, *cQ = sQ + kb * C * CK, *cV = sV + kb * C * CV;
+        // the inputs landed (already observed by the prep warps; re-checked, bounded)
+        if (!mbar_wait(&mbar[kb], (unsigned)((c / 3) & 1), kWaitTries) && lane == 0)
+            atomicAdd(&g_prefill_wait_timeouts, 1u);
+        const uint4 *cK = sK + kb * KH * BOXU, *cQ = sQ + kb * KH * BOXU, *cV = sV + kb * VH * BOXU;
+        uint4 *cO = sO + ob * VH * BOXU;
         const float *gam = sgam[pb], *dec = sdec[pb];
 #pragma unroll 1
         for (int j = 0; j < NSUB; ++j) {
@@ -369,8 +403,8 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 unsigned bk[4], bq[4];
                 const int r = 16 * j + (lane & 7) + ((lane >> 4) << 3);
                 const int cc = 2 * ks + ((lane >> 3) & 1);
-                ldsm_x4(bk, cK + hsw<CK>(r, cc));
-                ldsm_x4(bq, cQ + hsw<CK>(r, cc));
+                ldsm_x4(bk, cK + box_chunk(C, r, cc));
+                ldsm_x4(bq, cQ + box_chunk(C, r, cc));
                 const unsigned k0[2] = {bk[0], bk[1]}, k1[2] = {bk[2], bk[3]};
                 const unsigned q0[2] = {bq[0], bq[1]}, q1[2] = {bq[2], bq[3]};
                 mma_16816(X[0], aS[ks], k0);
@@ -379,8 +413,8 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(X[3], aS[ks], q1);
             }
             unsigned vt[4];
-            ldsm_x4_t(vt, cV + hsw<CV>(16 * j + ((lane >> 4) << 3) + (lane & 7),
-                                       (i0 >> 3) + ((lane >> 3) & 1)));
+            ldsm_x4_t(vt, cV + box_chunk(C, 16 * j + ((lane >> 4) << 3) + (lane & 7),
+                                         (i0 >> 3) + ((lane >> 3) & 1)));
             float R[2][4], Dl[2][4], O[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {  // R = V^T - gam X_K ; O starts at gam X_Q
@@ -413,9 +447,9 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 mma_16816(O[0], aD, m0);
                 mma_16816(O[1], aD, m1);
             }
-            {   // O^T tile -> sO[t][i] (16-byte chunks swizzled by t & 7)
+            {   // O^T tile -> O box rows t (token), columns i (dv)
                 const int m = lane >> 3, t = 16 * j + 8 * (m >> 1) + (lane & 7);
-                stsm_x4_t(reinterpret_cast<uint4 *>(sO) + t * CV + (((i0 >> 3) + (m & 1)) ^ (t & 7)),
+                stsm_x4_t(cO + box_chunk(C, t, (i0 >> 3) + (m & 1)),
                           pack_h2(O[0][0], O[0][1]), pack_h2(O[0][2], O[0][3]),
                           pack_h2(O[1][0], O[1][1]), pack_h2(O[1][2], O[1][3]));
             }
@@ -443,8 +477,8 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
 #pragma unroll
                 for (int c2 = 0; c2 < NTK / 2; ++c2) {
                     unsigned bk[4];
-                    ldsm_x4_t(bk, cK + hsw<CK>(16 * j + (lane & 7) + (((lane >> 3) & 1) << 3),
-                                               2 * c2 + (lane >> 4)));
+                    ldsm_x4_t(bk, cK + box_chunk(C, 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3),
+                                                 2 * c2 + (lane >> 4)));
                     const unsigned b0[2] = {bk[0], bk[1]}, b1[2] = {bk[2], bk[3]};
                     mma_16816(DS[2 * c2], aT, b0);
                     mma_16816(DS[2 * c2 + 1], aT, b1);
@@ -452,7 +486,10 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
             }
         }
         if (c + 2 < nchunks) bar_arrive(kBarEmpty + pb, NTALL);  // inputs / products of chunk c consumed
-        if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged in shared
+        // The previous chunk's TMA stores have read the checkpoint box (and O boxes).
+        if (tid == 0) bulk_wait_read();
+        bar_sync(kBarChain, NTC);
+        if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged for the TMA store
 #pragma unroll
             for (int c2 = 0; c2 < NTK / 2; ++c2) {
                 unsigned r[4];
@@ -468,23 +505,20 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
                 }
                 // matrices: rows 0-7 / 8-15 of dk columns 16c2.., then of 16c2+8..
                 const int m = lane >> 3, row = i0 + (m & 1) * 8 + (lane & 7);
-                stsm_x4(sCk + row * CK + ((2 * c2 + (m >> 1)) ^ (row & 7)), r[0], r[1], r[2], r[3]);
+                stsm_x4(sCk + box_chunk(DV, row, 2 * c2 + (m >> 1)), r[0], r[1], r[2], r[3]);
             }
         }
-        bar_sync(kBarChain, NTC);  // the O tile (and the checkpoint tile) are complete
-        for (int i = tid; i < nc * CV; i += NTC) {
-            const int t = i / CV, ch = i % CV;
-            *reinterpret_cast<uint4 *>(out + ((n * P + p0 + t) * H + h) * DV + ch * 8) =
-                reinterpret_cast<const uint4 *>(sO)[t * CV + (ch ^ (t & 7))];
-        }
-        if (nc == C) {
-            uint4 *dst = reinterpret_cast<uint4 *>(ckpt + ((n * nfull + c) * H + h) * set_elems);
-            for (int i = tid; i < DV * CK; i += NTC) {
-                const int row = i / CK, ch = i % CK;
-                __stcs(dst + i, sCk[row * CK + (ch ^ (row & 7))]);
-            }
+        fence_proxy_async();
+        bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
+        if (tid == 0) {
+            for (int x = 0; x < VH; ++x) tma_store_4d(&maps.o, 64 * x, h, p0, n, cO + x * BOXU);
+            if (nc == C)
+                for (int x = 0; x < KH; ++x)
+                    tma_store_3d(&maps.ck, 64 * x, 0, (n * nfull + c) * H + h, sCk + x * DV * 8);
+            bulk_commit();
         }
     }
+    if (tid == 0) bulk_wait();
 #pragma unroll
     for (int nt = 0; nt < NTK; ++nt) {
         *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc) =
@@ -492,6 +526,34 @@ prefill_wy_kernel(int H, int P, const __half *__restrict__ q, const __half *__re
         *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc) =
             __floats2half2_rn(DS[nt][2], DS[nt][3]);
     }
+}
+
+// cuTensorMapEncodeTiled from the driver (no link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// fp16 tensor map over `rank` dims (innermost first), 64-column boxes, 128-byte swizzle.
+bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+               strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int DK, int DV>
@@ -508,10 +570,30 @@ dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, c
         }
         configured = true;
     }
+    PrefillMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (P > 0) {
+        // q, k [N][P][H][DK], v, out [N][P][H][DV] as 4-d (d, head, token, sequence)
+        const cuuint64_t dk_dims[4] = {(cuuint64_t)DK, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)N};
+        const cuuint64_t dk_str[3] = {(cuuint64_t)DK * 2, (cuuint64_t)H * DK * 2, (cuuint64_t)P * H * DK * 2};
+        const cuuint64_t dv_dims[4] = {(cuuint64_t)DV, (cuuint64_t)H, (cuuint64_t)P, (cuuint64_t)N};
+        const cuuint64_t dv_str[3] = {(cuuint64_t)DV * 2, (cuuint64_t)H * DV * 2, (cuuint64_t)P * H * DV * 2};
+        const cuuint32_t box4[4] = {64, 1, 64, 1};
+        if (!encode_map(&maps.q, q, 4, dk_dims, dk_str, box4) ||
+            !encode_map(&maps.k, k, 4, dk_dims, dk_str, box4) ||
+            !encode_map(&maps.v, v, 4, dv_dims, dv_str, box4) ||
+            !encode_map(&maps.o, out, 4, dv_dims, dv_str, box4))
+            return DN_ERR_CUDA;
+    }
+    if (P >= 64) {
+        // ckpt [N][P/64][H][DV][DK] as 3-d (dk, dv, checkpoint tile)
+        const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)DV, (cuuint64_t)N * (P / 64) * H};
+        const cuuint64_t str[2] = {(cuuint64_t)DK * 2, (cuuint64_t)DV * DK * 2};
+        const cuuint32_t box3[3] = {64, (cuuint32_t)DV, 1};
+        if (!encode_map(&maps.ck, ckpt, 3, dims, str, box3)) return DN_ERR_CUDA;
+    }
     prefill_wy_kernel<DK, DV><<<(unsigned)((long long)N * H), DV * 2 + kPrepThreads, bytes, st>>>(
-        H, P, static_cast<const __half *>(q), static_cast<const __half *>(k),
-        static_cast<const __half *>(v), beta, g, static_cast<const __half *>(s_in),
-        static_cast<__half *>(out), static_cast<__half *>(ckpt), static_cast<__half *>(s_out));
+        H, P, maps, beta, g, static_cast<const __half *>(s_in), static_cast<__half *>(s_out));
     return DN_OK;
 }
 
@@ -531,6 +613,15 @@ void launch_prefill_seq(int N, int H, int P, int chunk, int dv, const void *q, c
 
 }  // namespace
 }  // namespace dn
+
+extern "C" unsigned int dn_prefill_wait_timeouts(void) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, dn::g_prefill_wait_timeouts, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0xffffffffu;
+    }
+    return v;
+}
 
 extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int dk, int dv,
                                            dn_dtype io_dt, dn_dtype state_dt, const void *q,

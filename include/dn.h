@@ -237,6 +237,17 @@ dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logit_dt, const
                                    const int32_t *draft_ids, int32_t *target_ids,
                                    int32_t *accepted_len, dn_stream_t stream);
 
+/*
+ * dn_prefill_wait_timeouts -- diagnostics of the fp16 prefill kernel.
+ *
+ * The fp16 prefill streams its inputs with the GPU's tensor-copy engine and waits
+ * for them with bounded polls; a wait that runs out is counted (never a hang), and
+ * the results of that call are invalid. Returns how many waits ran out since the
+ * library was loaded on the current device (0 in correct operation), or
+ * 0xffffffff if the counter could not be read. Synchronises the current device.
+ */
+unsigned int dn_prefill_wait_timeouts(void);
+
 /* Static, NUL-terminated description of a status code. */
 const char *dn_status_string(dn_status s);
 

@@ -93,3 +93,11 @@ def test_prefill_equals_verify_blocks_chained(cuda):
         s = c[:, -1].contiguous()
     torch.testing.assert_close(s, s_out, rtol=0, atol=1e-5)
     torch.testing.assert_close(s, ckpt[:, 0], rtol=0, atol=1e-5)
+
+
+def test_no_input_wait_ran_out(cuda):
+    # the bounded input waits of the fp16 prefill never gave up in this process
+    x = inputs.recurrence_inputs(2, 300, 4, 128, 128, seed=500, device=cuda)
+    dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
+    torch.cuda.synchronize()
+    assert dn.dn_prefill_wait_timeouts() == 0

@@ -60,6 +60,23 @@ def prefill_bytes(N, P, H, dk, dv, esz, chunk=64):
     return N * H * per_head
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(value, dist, device):
+    """The largest `value` over all ranks (the job's duration is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base, rank, buffer_set):
+    """Seed of a rank's buffer set: every rank verifies its own requests."""
+    return base + 1000 * rank + 17 * buffer_set
+
+
 # ----------------------------------------------------------------------------- environment
 
 def peaks():
@@ -168,7 +185,7 @@ def make_step_sets(w, device, rank, count):
     N, B, T = w["L"] * w["B"], w["B"], w["T"]
     sets = []
     for r in range(count):
-        seed = w["seed"] + 1000 * rank + 17 * r
+        seed = rank_seed(w["seed"], rank, r)
         x = inputs.recurrence_inputs(N, T, w["H"], w["dk"], w["dv"], io=w["io"], state=w["state"],
                                      seed=seed, device=device)
         logits, target = inputs.logits_inputs(B, T, w["V"], dtype=w["logit_dtype"],
@@ -462,10 +479,7 @@ def main():
     time.sleep(0.3)
 
     secs, per, (tw0, tw1) = timed_steps(sets, args.steps, args.warmup, stream, dist)
-    if dist is not None:
-        t = torch.tensor([secs], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+    secs = max_over_ranks(secs, dist, device)
     units_per_rank = B * T * w["L"] * args.steps
     value = units_per_rank * world / secs
 

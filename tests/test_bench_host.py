@@ -1,0 +1,95 @@
+"""Host-side logic of bench.py on CPU: multi-rank timing over gloo, byte accounting,
+clock-sample parsing and the peak fallback (no GPU)."""
+
+import os
+import socket
+import time
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # each rank's own duration; the job takes the slowest
+        got = bench.max_over_ranks(0.5 + rank, dist, torch.device("cpu"))
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_world_size_2_gloo():
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        assert dict(out) == {0: 1.5, 1: 1.5}
+
+
+def test_max_over_ranks_single_process_is_identity():
+    assert bench.max_over_ranks(0.25, None, None) == 0.25
+
+
+def test_rank_seeds_differ_per_rank_and_set():
+    seeds = {bench.rank_seed(1001, r, b) for r in range(8) for b in range(3)}
+    assert len(seeds) == 24
+
+
+def test_verify_bytes_single_user_launch():
+    # 48 layers x 48 heads: state 32 KiB + 16 x (q,k,v,o 4 x 256 B) + 16 x 8 B + 16 x 32 KiB
+    per_head = 32768 + 16 * 1024 + 128 + 16 * 32768
+    assert bench.verify_bytes(48, 16, 48, 128, 128, 2) == 48 * 48 * per_head == 1321500672
+
+
+def test_commit_and_accept_bytes():
+    acc = torch.tensor([15])
+    assert bench.commit_bytes(48, acc, 48, 128, 128, 2) == 2 * 48 * 48 * 128 * 128 * 2
+    assert bench.commit_bytes(48, torch.tensor([0]), 48, 128, 128, 2) == 0
+    assert bench.accept_bytes(1, 16, 151936, 2) == 16 * 151936 * 2 + 16 * 8 + 4
+
+
+def test_prefill_bytes_25k():
+    # q, k, v, o + beta, g per token-head, state in + out, one checkpoint per 64 tokens
+    b = bench.prefill_bytes(1, 25000, 48, 128, 128, 2)
+    per_head = 25000 * (4 * 256 + 8) + 2 * 32768 + 390 * 32768
+    assert b == 48 * per_head
+
+
+def test_peaks_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 6696.2}')
+    assert bench.peaks() == (6696.2, "measured")
+
+
+def test_clock_sampler_summary_parsing():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    t0 = time.time()
+    stamp = lambda dt: time.strftime("%Y/%m/%d %H:%M:%S", time.localtime(t0 + dt)) + ".100"
+    cs.lines = [
+        "%s, 0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active" % stamp(0),
+        "%s, 0, 1980, 2070, 1300.5, 0x4, Not Active, Not Active, Not Active, Active" % stamp(1),
+        "%s, 1, 345, 2070, 90.0, 0x0, Not Active, Not Active, Not Active, Not Active" % stamp(1),
+    ]
+    s = cs.summary(t0 - 1, t0 + 2, 0)
+    assert s["sm_mhz"] == pytest.approx((2070 + 1980) / 2)
+    assert s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def test_kernel_sources_hash_is_stable():
+    assert bench.kernel_sources_hash() == bench.kernel_sources_hash()

@@ -166,18 +166,18 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
 // Shared-memory tiles. q/k/v, O and the checkpoint move with the tensor-map (TMA) engine
 // in 64-column boxes of 128-byte rows, swizzled by the engine: 16-byte chunk c of row r
 // of a box sits at chunk c ^ (r & 7). Every box starts on a 1024-byte boundary.
-template <int DK, int DV>
+template <int DK, int DVC>
 struct PrefillSmem {
     static constexpr int C = 64, NSUB = 4, NKQV = 3, NPREP = 2;
-    static constexpr int KH = DK / 64, VH = DV / 64;    // 64-column boxes per row
+    static constexpr int KH = DK / 64, VH = DVC / 64;   // 64-column boxes per row
     static constexpr size_t kBox = (size_t)C * 128;      // one 64 x 64 fp16 box
     // byte offsets
     static constexpr size_t kK = 0;                                       // [3][KH] boxes
     static constexpr size_t kQ = kK + (size_t)NKQV * KH * kBox;
     static constexpr size_t kV = kQ + (size_t)NKQV * KH * kBox;          // [3][VH] boxes
     static constexpr size_t kO = kV + (size_t)NKQV * VH * kBox;          // [2][VH] boxes
-    static constexpr size_t kCk = kO + (size_t)2 * VH * kBox;            // [KH] boxes of DV rows
-    static constexpr size_t kTb = kCk + (size_t)KH * DV * 128;           // [2][NSUB][16][24] half
+    static constexpr size_t kCk = kO + (size_t)2 * VH * kBox;            // [KH] boxes of DVC rows
+    static constexpr size_t kTb = kCk + (size_t)KH * DVC * 128;          // [2][NSUB][16][24] half
     static constexpr size_t kMq = kTb + NPREP * NSUB * 16 * 24 * 2;      // [2][NSUB][16][24] half
     static constexpr size_t kGam = kMq + NPREP * NSUB * 16 * 24 * 2;     // [2][C] float
     static constexpr size_t kDec = kGam + NPREP * C * 4;                 // [2][C] float
@@ -193,7 +193,10 @@ __device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
     return (ch >> 3) * rows * 8 + r * 8 + ((ch & 7) ^ (r & 7));
 }
 
-// Warp roles. Chain warps (DV/16 of them, 16 dv-rows each) hold the state and run
+// A CTA owns DVC of the DV rows of one (sequence, head) state: all of them, or half when
+// there are fewer (sequence, head) pairs than SMs (each half then repeats the
+// state-independent work, which idle SMs absorb).
+// Warp roles. Chain warps (DVC/16 of them, 16 dv-rows each) hold the state and run
 // the state-dependent steps of chunk c; four prep warps meanwhile load chunk c+1 and
 // compute its state-independent products. Hand-off per chunk parity p with named
 // barriers over all threads: FULL[p] (prep arrives, chain waits) when chunk c's
@@ -211,14 +214,14 @@ struct PrefillMaps {
     CUtensorMap q, k, v, o, ck;
 };
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(DV * 2 + kPrepThreads, 1)
+template <int DK, int DV, int DVC>
+__global__ void __launch_bounds__(DVC * 2 + kPrepThreads, 1)
 prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                   const float *__restrict__ beta, const float *__restrict__ g,
                   const __half *s_in, __half *s_out) {
-    using L = PrefillSmem<DK, DV>;
+    using L = PrefillSmem<DK, DVC>;
     constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
-    constexpr int NW = DV / 16, NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
+    constexpr int NW = DVC / 16, NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
     constexpr int BOXU = C * 8;   // uint4 per 64 x 64 box
@@ -236,8 +239,11 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     float(*sGates)[2][C] = reinterpret_cast<float(*)[2][C]>(smem + L::kGates);  // [buf][beta|g][t]
     unsigned long long *mbar = reinterpret_cast<unsigned long long *>(smem + L::kMbar);
 
-    const int h = blockIdx.x % H;
-    const int n = blockIdx.x / H;
+    constexpr int RB = DV / DVC;  // CTAs per (sequence, head)
+    const int rb = blockIdx.x % RB;
+    const int h = (blockIdx.x / RB) % H;
+    const int n = blockIdx.x / (RB * H);
+    const int r0 = rb * DVC;      // first state row of this CTA
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int fr = lane >> 2, fc = 2 * (lane & 3);  // fragment row / column pair
     const size_t set_elems = (size_t)DV * DK;
@@ -265,7 +271,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                     tma_load_4d(sQ + (kb * KH + x) * BOXU, &maps.q, 64 * x, h, p0, n, &mbar[kb]);
                 }
                 for (int x = 0; x < VH; ++x)
-                    tma_load_4d(sV + (kb * VH + x) * BOXU, &maps.v, 64 * x, h, p0, n, &mbar[kb]);
+                    tma_load_4d(sV + (kb * VH + x) * BOXU, &maps.v, r0 + 64 * x, h, p0, n, &mbar[kb]);
             }
             const size_t row0 = ((size_t)n * P + p0) * H + h;
             for (int i = pt; i < 2 * C; i += NTP) {
@@ -366,16 +372,16 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
 
     // ============================== chain warps ==============================
-    const int i0 = warp * 16;  // this warp's dv rows
+    const int i0 = warp * 16;  // this warp's rows within the CTA (state rows r0 + i0 ..)
     float DS[NTK][4];          // state tile nt: dk columns 8nt .. 8nt+7 of rows i0 .. i0+15
 #pragma unroll
     for (int nt = 0; nt < NTK; ++nt) {
         float2 lo = make_float2(0.f, 0.f), hi = lo;
         if (s_in) {
             lo = __half22float2(*reinterpret_cast<const __half2 *>(
-                s_in + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc));
+                s_in + state_off + (size_t)(r0 + i0 + fr) * DK + 8 * nt + fc));
             hi = __half22float2(*reinterpret_cast<const __half2 *>(
-                s_in + state_off + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc));
+                s_in + state_off + (size_t)(r0 + i0 + fr + 8) * DK + 8 * nt + fc));
         }
         DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
     }
@@ -505,25 +511,25 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 }
                 // matrices: rows 0-7 / 8-15 of dk columns 16c2.., then of 16c2+8..
                 const int m = lane >> 3, row = i0 + (m & 1) * 8 + (lane & 7);
-                stsm_x4(sCk + box_chunk(DV, row, 2 * c2 + (m >> 1)), r[0], r[1], r[2], r[3]);
+                stsm_x4(sCk + box_chunk(DVC, row, 2 * c2 + (m >> 1)), r[0], r[1], r[2], r[3]);
             }
         }
         fence_proxy_async();
         bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
         if (tid == 0) {
-            for (int x = 0; x < VH; ++x) tma_store_4d(&maps.o, 64 * x, h, p0, n, cO + x * BOXU);
+            for (int x = 0; x < VH; ++x) tma_store_4d(&maps.o, r0 + 64 * x, h, p0, n, cO + x * BOXU);
             if (nc == C)
                 for (int x = 0; x < KH; ++x)
-                    tma_store_3d(&maps.ck, 64 * x, 0, (n * nfull + c) * H + h, sCk + x * DV * 8);
+                    tma_store_3d(&maps.ck, 64 * x, r0, (n * nfull + c) * H + h, sCk + x * DVC * 8);
             bulk_commit();
         }
     }
     if (tid == 0) bulk_wait();
 #pragma unroll
     for (int nt = 0; nt < NTK; ++nt) {
-        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr) * DK + 8 * nt + fc) =
+        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + fr) * DK + 8 * nt + fc) =
             __floats2half2_rn(DS[nt][0], DS[nt][1]);
-        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(i0 + fr + 8) * DK + 8 * nt + fc) =
+        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + fr + 8) * DK + 8 * nt + fc) =
             __floats2half2_rn(DS[nt][2], DS[nt][3]);
     }
 }
@@ -556,14 +562,24 @@ bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *di
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DK, int DV>
-dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
-                            const float *beta, const float *g, const void *s_in, void *out,
-                            void *ckpt, void *s_out, cudaStream_t st) {
-    constexpr size_t bytes = PrefillSmem<DK, DV>::kBytes;
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
+template <int DK, int DV, int DVC>
+dn_status launch_prefill_wy_split(int N, int H, int P, const void *q, const void *k, const void *v,
+                                  const float *beta, const float *g, const void *s_in, void *out,
+                                  void *ckpt, void *s_out, cudaStream_t st) {
+    constexpr size_t bytes = PrefillSmem<DK, DVC>::kBytes;
     static bool configured = false;  // the attribute is per function and idempotent
     if (!configured) {
-        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, DVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess) {
             cudaGetLastError();
             return DN_ERR_CUDA;
@@ -586,15 +602,25 @@ dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, c
             return DN_ERR_CUDA;
     }
     if (P >= 64) {
-        // ckpt [N][P/64][H][DV][DK] as 3-d (dk, dv, checkpoint tile)
+        // ckpt [N][P/64][H][DV][DK] as 3-d (dk, dv, checkpoint tile); a box is DVC rows
         const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)DV, (cuuint64_t)N * (P / 64) * H};
         const cuuint64_t str[2] = {(cuuint64_t)DK * 2, (cuuint64_t)DV * DK * 2};
-        const cuuint32_t box3[3] = {64, (cuuint32_t)DV, 1};
+        const cuuint32_t box3[3] = {64, (cuuint32_t)DVC, 1};
         if (!encode_map(&maps.ck, ckpt, 3, dims, str, box3)) return DN_ERR_CUDA;
     }
-    prefill_wy_kernel<DK, DV><<<(unsigned)((long long)N * H), DV * 2 + kPrepThreads, bytes, st>>>(
+    prefill_wy_kernel<DK, DV, DVC><<<(unsigned)((long long)N * H * (DV / DVC)), DVC * 2 + kPrepThreads, bytes,
+                                      st>>>(
         H, P, maps, beta, g, static_cast<const __half *>(s_in), static_cast<__half *>(s_out));
     return DN_OK;
+}
+
+template <int DK, int DV>
+dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, const void *v,
+                            const float *beta, const float *g, const void *s_in, void *out,
+                            void *ckpt, void *s_out, cudaStream_t st) {
+    if (DV == 128 && (long long)N * H < sm_count())
+        return launch_prefill_wy_split<DK, DV, 64>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
+    return launch_prefill_wy_split<DK, DV, DV>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
 }
 
 constexpr int kRows = 16;

@@ -101,3 +101,25 @@ def test_no_input_wait_ran_out(cuda):
     dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
     torch.cuda.synchronize()
     assert dn.dn_prefill_wait_timeouts() == 0
+
+
+def test_whole_and_half_row_ctas_agree(cuda):
+    # N*H >= the SM count runs one CTA per (sequence, head); a single sequence runs two
+    # CTAs per head (half the rows each). Same arithmetic per row: bit-identical results.
+    N, P, H, d = 4, 130, 48, 128
+    assert N * H >= torch.cuda.get_device_properties(0).multi_processor_count
+    x = inputs.recurrence_inputs(N, P, H, d, d, seed=600, device=cuda)
+    o_all, c_all, s_all = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
+    for n in range(N):
+        xs = [x[k][n:n + 1].contiguous() for k in KEYS]
+        o1, c1, s1 = dn.dn_prefill_checkpoint(*xs, x["state"][n:n + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o_all[n:n + 1]) and torch.equal(c1, c_all[n:n + 1])
+        assert torch.equal(s1, s_all[n:n + 1])
+    heads = [0, 47]
+    u = {k: np64(x[k][:1, :, heads]) for k in KEYS}
+    ref = oracle.prefill_checkpoint(u["q"], u["k"], u["v"], u["beta"], u["g"],
+                                    np64(x["state"][:1, heads]), chunk=64, store="f16", io="f16")
+    assert_close("out", o_all[:1, :, heads], ref[0], TOL["f16"])
+    assert_close("ckpt", c_all[:1, :, heads], ref[1], TOL["f16"])
+    assert_close("state_out", s_all[:1, heads], ref[2], TOL["f16"])

@@ -89,10 +89,12 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_hash():
+def kernel_sources_hash(files=None):
+    """Hash of the kernel sources (all of csrc, or the named files) the counters were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deltanet_recurrent_state_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = sorted(files) if files else sorted(os.listdir(csrc))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -100,17 +102,17 @@ def kernel_sources_hash():
 
 def ncu_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
-    kernel sources changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "ncu_counters.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("sources_sha256_16") != kernel_sources_hash():
-        return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch_full")
+    if k is None or k.get("sources_sha256_16") != kernel_sources_hash(k.get("sources")):
+        return None
+    return k.get("dram_bytes_per_launch_full")
 
 
 class ClockSampler:

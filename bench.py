@@ -54,6 +54,21 @@ def commit_bytes(L, acc, H, dk, dv, esz):
     return 2 * L * int((acc >= 1).sum()) * H * dv * dk * esz
 
 
+def verify_deltas_bytes(N, T, H, dk, dv, esz):
+    """dn_verify_block_deltas: read state, q, k, v, beta, g; write out and delta (fp32)."""
+    return N * H * (dv * dk * esz + T * (2 * dk + 2 * dv) * esz + T * 8 + T * dv * 4)
+
+
+def commit_deltas_bytes(L, acc, H, dk, dv, esz):
+    """dn_commit_deltas: per (layer, request) with a >= 1 read and write the state, read
+    a keys, gates and deltas."""
+    total = 0
+    for a in acc.tolist():
+        if a >= 1:
+            total += L * H * (2 * dv * dk * esz + a * (dk * esz + 4 + dv * 4))
+    return total
+
+
 def prefill_bytes(N, P, H, dk, dv, esz, chunk=64):
     per_head = (P * (2 * dk + 2 * dv) * esz + P * 8 + 2 * dv * dk * esz +
                 (P // chunk) * dv * dk * esz)
@@ -346,6 +361,58 @@ def prefill_row(device, stream, reps=2):
             "algorithmic_bytes": nbytes}
 
 
+def deltas_row(sets, device, stream, steps=200, warmup=5):
+    """The single-user step with recompute on commit: verify without checkpoints (delta_t
+    per row instead), greedy accept, commit rebuilding the accepted state from delta."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS[HEADLINE]
+    N, B, T, H, dk, dv = w["L"] * w["B"], w["B"], w["T"], w["H"], w["dk"], w["dv"]
+    for x in sets:
+        x["delta"] = torch.empty((N, T, H, dv), dtype=torch.float32, device=device)
+
+    def step(x, evs=None):
+        if evs:
+            evs[0].record(stream)
+        dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                                  x["delta"], stream=stream)
+        if evs:
+            evs[1].record(stream)
+        dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+        if evs:
+            evs[2].record(stream)
+        dn.dn_commit_deltas(x["k"], x["g"], x["delta"], x["acc"], x["state"], stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(sets[i % len(sets)])
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(sets[i % len(sets)], evs[i])
+    s1.record(stream)
+    torch.cuda.synchronize()
+    secs = s0.elapsed_time(s1) / 1e3
+    per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(3)]
+    vb = verify_deltas_bytes(N, T, H, dk, dv, 2)
+    cb = commit_deltas_bytes(w["L"], sets[0]["acc_plan"], H, dk, dv, 2)
+    for x in sets:
+        del x["delta"]
+    return {"workload": HEADLINE + " (recompute on commit)", "ms_per_step": secs / steps * 1e3,
+            "token_layers_per_s": B * T * w["L"] * steps / secs,
+            "verify_deltas_ms": per[0], "verify_deltas_gbs": vb / (per[0] / 1e3) / 1e9,
+            "accept_ms": per[1], "commit_deltas_ms": per[2],
+            "commit_deltas_gbs": cb / (per[2] / 1e3) / 1e9,
+            "state_pages_per_request_layer": "1 (+ fp32 deltas: T x H x dv x 4 B) instead of T + 1",
+            "algorithmic_bytes_per_step": vb + cb + accept_bytes(B, T, w["V"], 2)}
+
+
 def batch_row(device, stream, steps=10, warmup=3):
     from deltanet_recurrent_state_gb300.workloads import WORKLOADS
     w = WORKLOADS["batch64_l48_h48_d128_t4_f16"]
@@ -491,6 +558,7 @@ def main():
 
     rows = {}
     if not args.no_rows and rank == 0:
+        rows["recompute_on_commit_step"] = deltas_row(sets, device, stream)
         rows["batch64_step"] = batch_row(device, stream)
         rows["prefill"] = prefill_row(device, stream)
     clocks.stop()

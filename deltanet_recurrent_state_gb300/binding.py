@@ -34,6 +34,8 @@ SIGNATURES = {
     "dn_status_string": (ctypes.c_char_p, [_I]),
     "dn_accept_greedy_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dn_prefill_wait_timeouts": (ctypes.c_uint, []),
+    "dn_verify_block_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "dn_commit_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -115,6 +117,38 @@ def dn_verify_block(q, k, v, beta, g, state_in, out=None, ckpt=None, stream=None
         _ptr(beta), _ptr(g), _ptr(state_in), _ptr(out), _ptr(ckpt), _stream(stream))
     _check("dn_verify_block", st)
     return out, ckpt
+
+
+def dn_verify_block_deltas(q, k, v, beta, g, state_in, out=None, delta=None, stream=None):
+    """As dn_verify_block, but writes delta [N,T,H,dv] fp32 instead of checkpoints."""
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
+    if delta is None:
+        delta = torch.empty((N, T, H, dv), dtype=torch.float32, device=q.device)
+    _dev(q, k, v, beta, g, state_in, out, delta)
+    assert k.shape == q.shape and v.shape == (N, T, H, dv) and state_in.shape == (N, H, dv, dk)
+    assert delta.shape == (N, T, H, dv) and delta.dtype == torch.float32
+    st = load_library().dn_verify_block_deltas(
+        N, H, T, dk, dv, _DT[q.dtype], _DT[state_in.dtype], _ptr(q), _ptr(k), _ptr(v),
+        _ptr(beta), _ptr(g), _ptr(state_in), _ptr(out), _ptr(delta), _stream(stream))
+    _check("dn_verify_block_deltas", st)
+    return out, delta
+
+
+def dn_commit_deltas(k, g, delta, accepted_len, state, stream=None):
+    """Rebuild the accepted state in place from delta [N,T,H,dv], k [N,T,H,dk], g [N,T,H]."""
+    N, H, dv, dk = state.shape
+    T = k.shape[1]
+    B = accepted_len.shape[0]
+    _dev(k, g, delta, accepted_len, state)
+    assert k.shape == (N, T, H, dk) and g.shape == (N, T, H) and delta.shape == (N, T, H, dv)
+    st = load_library().dn_commit_deltas(N, B, H, T, dk, dv, _DT[state.dtype], _ptr(k), _ptr(g),
+                                         _ptr(delta), _ptr(accepted_len), _ptr(state),
+                                         _stream(stream))
+    _check("dn_commit_deltas", st)
+    return state
 
 
 def dn_accept_workspace_bytes(B, T, V):

@@ -152,12 +152,14 @@ __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
     return u;
 }
 
-template <int DK>
+// CKPT: write the T checkpoints (dn_verify_block); otherwise write delta_t instead
+// (dn_verify_block_deltas), from which dn_commit_deltas rebuilds the accepted state.
+template <int DK, bool CKPT>
 __global__ void __launch_bounds__(256, 5)
 verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
                  const __half *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ g, const __half *__restrict__ s_in,
-                 __half *__restrict__ out, __half *__restrict__ ckpt) {
+                 __half *__restrict__ out, __half *__restrict__ ckpt, float *__restrict__ delta) {
     constexpr int ROWS = 32, TPR = 8, NT = 256;
     constexpr int CPR = DK / 8;        // 16-byte chunks per row
     constexpr int NCH = CPR / TPR;     // chunks per lane
@@ -300,10 +302,16 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     }
     __syncthreads();
 
+    if (!CKPT) {  // 5'. delta_t for the rows of this CTA: [N][T][H][DV] fp32
+        for (int i = tid; i < T * ROWS; i += NT) {
+            const int t = i / ROWS, r = i % ROWS;
+            delta[((n * T + t) * H + h) * DV + rb * ROWS + r] = sd[t][r];
+        }
+    }
     // 5. checkpoints S_t = g_t S_{t-1} + delta_t k_t^T
-    __half *dst = ckpt + ((n * T) * H + h) * set_elems + (size_t)row * DK + ln * 8;
+    __half *dst = CKPT ? ckpt + ((n * T) * H + h) * set_elems + (size_t)row * DK + ln * 8 : nullptr;
     const size_t tstride = (size_t)H * set_elems;
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; CKPT && t < T; ++t) {
         const float dt = sd[t][lr], gt = sg[t];
         const float2 d2 = make_float2(dt, dt), g2 = make_float2(gt, gt);
         const float4 *k4 = reinterpret_cast<const float4 *>(sk[t]);
@@ -374,12 +382,40 @@ extern "C" dn_status dn_verify_block(int N, int H, int T, int dk, int dv, dn_dty
         const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
         __half *oh = static_cast<__half *>(out), *ch = static_cast<__half *>(ckpt);
         if (dk == 128)
-            verify_wy_kernel<128><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch);
+            verify_wy_kernel<128, true><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
         else
-            verify_wy_kernel<64><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch);
+            verify_wy_kernel<64, true><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
     } else {
         if (dk == 128) launch_verify<128, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
         else launch_verify<64, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
     }
+    return launch_status();
+}
+
+extern "C" dn_status dn_verify_block_deltas(int N, int H, int T, int dk, int dv, dn_dtype io_dt,
+                                            dn_dtype state_dt, const void *q, const void *k,
+                                            const void *v, const float *beta, const float *g,
+                                            const void *state_in, void *out, float *delta,
+                                            dn_stream_t stream) {
+    using namespace dn;
+    if (N < 0 || H < 1 || T < 1 || T > DN_MAX_BLOCK) return DN_ERR_INVALID_ARG;
+    if (!dtype_ok(io_dt) || !dtype_ok(state_dt)) return DN_ERR_INVALID_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv)) return DN_ERR_UNSUPPORTED;
+    if (io_dt != DN_F16 || state_dt != DN_F16) return DN_ERR_UNSUPPORTED;
+    if (N == 0) return DN_OK;
+    if (!q || !k || !v || !beta || !g || !state_in || !out || !delta) return DN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(state_in, 16) ||
+        !aligned(out, 16) || !aligned(delta, 16) || !aligned(beta, 4) || !aligned(g, 4))
+        return DN_ERR_INVALID_ARG;
+    if ((long long)N * H * (dv / kRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned blocks = (unsigned)((long long)N * H * (dv / kRows));
+    const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
+    const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
+    __half *oh = static_cast<__half *>(out);
+    if (dk == 128)
+        verify_wy_kernel<128, false><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+    else
+        verify_wy_kernel<64, false><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
     return launch_status();
 }

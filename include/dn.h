@@ -119,6 +119,40 @@ dn_status dn_verify_block(int N, int H, int T, int dk, int dv,
                           dn_stream_t stream);
 
 /*
+ * dn_verify_block_deltas / dn_commit_deltas -- the verify block without per-position
+ * checkpoints ("recompute on commit").
+ *
+ * A speculating request reserves a state copy per verified position ([P1]: 1.66 GiB
+ * at 15 drafts vs 0.88 GiB at 7; [P2]: "reserves recurrent-state pages"). This pair
+ * keeps none: verify writes, per position, only the write strength of the delta rule
+ *
+ *   delta_t = beta_t (v_t - g_t S_{t-1} k_t)        (one fp32 per state row)
+ *
+ * so that S_t = g_t S_{t-1} + delta_t k_t^T; commit then rebuilds the accepted state
+ * S_a from the old state, delta_0..delta_{a-1}, k and g, in place. The committed state
+ * is bit-identical to dn_verify_block + dn_commit on the same inputs; out is identical
+ * to dn_verify_block's.
+ *
+ * dn_verify_block_deltas: arguments as dn_verify_block, with
+ *   delta    [N][T][H][dv] fp32, 16-byte aligned, written (instead of ckpt)
+ * dn_commit_deltas: N, B, H, T, dk, dv, state_dt and accepted_len as dn_commit, with
+ *   k        [N][T][H][dk] the block's keys (io dtype), 16-byte aligned
+ *   g        [N][T][H] fp32 the block's gates
+ *   delta    [N][T][H][dv] fp32 from dn_verify_block_deltas
+ *   state    [N][H][dv][dk], updated in place (must be dn_verify_block_deltas' state_in)
+ * Both support the fp16 state / fp16 io pair only (DN_ERR_UNSUPPORTED otherwise).
+ */
+dn_status dn_verify_block_deltas(int N, int H, int T, int dk, int dv,
+                                 dn_dtype io_dt, dn_dtype state_dt,
+                                 const void *q, const void *k, const void *v,
+                                 const float *beta, const float *g,
+                                 const void *state_in, void *out, float *delta,
+                                 dn_stream_t stream);
+dn_status dn_commit_deltas(int N, int B, int H, int T, int dk, int dv, dn_dtype state_dt,
+                           const void *k, const float *g, const float *delta,
+                           const int32_t *accepted_len, void *state, dn_stream_t stream);
+
+/*
  * dn_accept_workspace_bytes -- device workspace dn_accept_greedy needs.
  * Returns 0 for B < 1, T < 1 or V < 1.
  */

@@ -1,0 +1,53 @@
+"""Recompute-on-commit (dn_verify_block_deltas + dn_commit_deltas) on the GPU: the same
+outputs and the same committed states, bit for bit, as the checkpoint path, and the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deltanet_recurrent_state_gb300 import binding as dn
+from deltanet_recurrent_state_gb300 import inputs
+from tests.parity import TOL, assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
+@pytest.mark.parametrize("T", [1, 7, 16])
+def test_deltas_path_equals_checkpoint_path(dk, dv, T, cuda):
+    L, B, H = 2, T + 1, 3          # request b accepts b tokens: every length 0..T
+    N = L * B
+    x = inputs.recurrence_inputs(N, T, H, dk, dv, seed=700 + T + dk + dv, device=cuda)
+    acc = torch.arange(B, dtype=torch.int32, device=cuda)
+    out_c, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    s_c = x["state"].clone()
+    dn.dn_commit(ckpt, acc, s_c)
+    out_d, delta = dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    s_d = x["state"].clone()
+    dn.dn_commit_deltas(x["k"], x["g"], delta, acc, s_d)
+    torch.cuda.synchronize()
+    assert torch.equal(out_d, out_c)
+    assert torch.equal(s_d, s_c)
+
+
+def test_deltas_commit_matches_oracle(cuda):
+    N, T, H, d = 3, 16, 4, 128
+    x = inputs.recurrence_inputs(N, T, H, d, d, seed=777, device="cpu")
+    g = {k: v.to(cuda) for k, v in x.items()}
+    acc = torch.tensor([5, 16, 0], dtype=torch.int32)
+    _, delta = dn.dn_verify_block_deltas(g["q"], g["k"], g["v"], g["beta"], g["g"], g["state"])
+    s = g["state"].clone()
+    dn.dn_commit_deltas(g["k"], g["g"], delta, acc.to(cuda), s)
+    torch.cuda.synchronize()
+    _, c_ref = oracle.verify_block(np64(x["q"]), np64(x["k"]), np64(x["v"]), np64(x["beta"]),
+                                   np64(x["g"]), np64(x["state"]), store="f16", io="f16")
+    ref = oracle.commit(np64(x["state"]), c_ref, acc.numpy())
+    assert_close("committed state", s, ref, TOL["f16"])
+
+
+def test_deltas_reject_fp32(cuda):
+    x = inputs.recurrence_inputs(1, 4, 2, 64, 64, io="f32", state="f32", seed=1, device=cuda)
+    with pytest.raises(dn.DnError) as e:
+        dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    assert e.value.status == dn.DN_ERR_UNSUPPORTED

@@ -36,6 +36,11 @@ SIGNATURES = {
     "dn_prefill_wait_timeouts": (ctypes.c_uint, []),
     "dn_verify_block_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dn_commit_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "dn_prefix_cache_create": (_P, [_I, _I]),
+    "dn_prefix_cache_destroy": (None, [_P]),
+    "dn_prefix_cache_insert": (_I, [_P, _P, _I, ctypes.c_int32, _P]),
+    "dn_prefix_cache_lookup": (_I, [_P, _P, _I, _P, _P]),
+    "dn_prefix_cache_size": (_I, [_P]),
 }
 
 
@@ -227,6 +232,56 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
 
 def dn_prefill_wait_timeouts():
     return int(load_library().dn_prefill_wait_timeouts())
+
+
+class PrefixCache:
+    """Host-side prefix index of state checkpoints (dn_prefix_cache_* in include/dn.h)."""
+
+    def __init__(self, capacity, chunk=PREFILL_CHUNK):
+        self._lib = load_library()
+        self._h = self._lib.dn_prefix_cache_create(chunk, capacity)
+        if not self._h:
+            raise ValueError("dn_prefix_cache_create failed")
+        self.chunk = chunk
+
+    @staticmethod
+    def _tokens(tokens):
+        import numpy as np
+        a = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return a, a.ctypes.data_as(ctypes.c_void_p)
+
+    def insert(self, tokens, position, slot):
+        """Record that the state after tokens[:position] is in `slot`; returns an evicted slot or -1."""
+        a, p = self._tokens(tokens)
+        if position > a.shape[0]:
+            raise ValueError("position beyond the tokens")
+        ev = ctypes.c_int32(-1)
+        _check("dn_prefix_cache_insert",
+               self._lib.dn_prefix_cache_insert(self._h, p, int(position), int(slot), ctypes.byref(ev)))
+        return ev.value
+
+    def lookup(self, tokens):
+        """(position, slot) of the longest cached prefix of `tokens`, (0, -1) if none."""
+        a, p = self._tokens(tokens)
+        pos, slot = ctypes.c_int(0), ctypes.c_int32(-1)
+        _check("dn_prefix_cache_lookup",
+               self._lib.dn_prefix_cache_lookup(self._h, p, int(a.shape[0]), ctypes.byref(pos),
+                                                ctypes.byref(slot)))
+        return pos.value, slot.value
+
+    def __len__(self):
+        return int(self._lib.dn_prefix_cache_size(self._h))
+
+    def close(self):
+        if self._h:
+            self._lib.dn_prefix_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dn_status_string(status):

@@ -120,3 +120,37 @@ def draft_ids(target, accepted, V, seed=0):
             off = int(torch.randint(1, V, (1,), generator=gen))
             d[b, a] = (tgt[b, a] + off) % V
     return d.to(torch.int32).to(target.device)
+
+
+def context_inputs(N, prompt_len, gen_len, vocab, quote=True, ragged=False, seed=0, device="cpu"):
+    """Token contexts for drafting from the request's own context.
+
+    Each row is a prompt of ``prompt_len`` tokens followed by ``gen_len`` generated
+    tokens. Prompt tokens are log-uniform over the vocabulary (P(t) proportional to
+    1/(t+1), a Zipf-like spread, so short repeats are common). With ``quote`` the
+    generated tokens are a verbatim copy of a uniformly placed passage of the prompt
+    (the document-reproduction case); otherwise they are fresh log-uniform tokens.
+    ``ragged`` draws each row's length uniformly from 0..prompt_len+gen_len; otherwise
+    every row is full. Returns (context [N, prompt_len + gen_len] int32, lengths [N] int32).
+    """
+    g = _gen(seed, "cpu")
+    Lmax = prompt_len + gen_len
+
+    def loguniform(shape):
+        u = torch.rand(shape, generator=g, dtype=torch.float64)
+        return (torch.exp(u * math.log(vocab + 1)).floor() - 1).clamp_(0, vocab - 1).to(torch.int32)
+
+    prompt = loguniform((N, prompt_len))
+    if quote and gen_len > 0:
+        if gen_len > prompt_len:
+            raise ValueError("a quoted passage cannot be longer than the prompt")
+        start = torch.randint(0, prompt_len - gen_len + 1, (N, 1), generator=g)
+        gen = torch.gather(prompt, 1, start + torch.arange(gen_len)[None, :])
+    else:
+        gen = loguniform((N, gen_len))
+    ctx = torch.cat([prompt, gen], dim=1).contiguous()
+    if ragged:
+        lengths = torch.randint(0, Lmax + 1, (N,), generator=g, dtype=torch.int32)
+    else:
+        lengths = torch.full((N,), Lmax, dtype=torch.int32)
+    return ctx.to(device), lengths.to(device)

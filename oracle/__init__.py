@@ -1,4 +1,5 @@
-"""CPU oracle for the DeltaNet verify / accept / commit / prefill-checkpoint path.
+"""CPU oracle for the DeltaNet verify / accept / commit / prefill-checkpoint path
+and for drafting from the request's own context.
 
 TEST INFRASTRUCTURE ONLY. This package is imported by ``tests/``, by
 ``__graft_entry__.smoke()`` and by the ``cpu_baseline`` / ``--impl reference``
@@ -26,6 +27,9 @@ Sources (cited by page title and section):
 * "HyperQwen on one RTX 3090: a first-time developer's guide to the 381-token
   claim", section "What actually became faster?": a verify block of up to 16
   tokens; prefix caching of a ~25,000-token document.
+* "HyperQwen: 1,000 tok/s ..." (Technical Insight) and "HyperQwen on one RTX 3090
+  ..." (What actually became faster?): later verify positions are drafted by copying
+  from the request's own context (``context_lookup.py`` states the reading used).
 * The pages name DeltaNet but never print its update. The update used here is
   the published gated delta rule (Yang, Kautz and Hatamizadeh, "Gated Delta
   Networks: Improving Mamba2 with Delta Rule", 2024):
@@ -45,3 +49,4 @@ from .recurrence import (  # noqa: F401
     prefill_checkpoint,
 )
 from .accept import argmax_lowest, accept_greedy  # noqa: F401
+from .context_lookup import context_drafts_row, context_drafts  # noqa: F401

@@ -53,3 +53,23 @@ def test_workload_table_shapes():
         assert w["dk"] in (64, 128) and w["dv"] in (64, 128), name
         if "T" in w:
             assert 1 <= w["T"] <= 16
+
+
+def test_context_inputs_quote_copies_a_prompt_passage():
+    ctx, lens = inputs.context_inputs(3, 500, 40, 151936, seed=5)
+    assert ctx.shape == (3, 540) and ctx.dtype == torch.int32 and (lens == 540).all()
+    assert int(ctx.min()) >= 0 and int(ctx.max()) < 151936
+    c = ctx.numpy()
+    for r in range(3):
+        gen = c[r, 500:].tolist()
+        assert any(c[r, s:s + 40].tolist() == gen for s in range(461))
+    again, _ = inputs.context_inputs(3, 500, 40, 151936, seed=5)
+    assert torch.equal(ctx, again)
+    # the quoted passage continues in the prompt: the oracle's drafts are that continuation
+    d, n, e = oracle.context_drafts_row(c[0], 4, 1, 8)
+    assert n == 4 and c[0, e - 4:e].tolist() == c[0, -4:].tolist()
+
+
+def test_context_inputs_ragged_lengths_in_range():
+    _, lens = inputs.context_inputs(200, 30, 10, 1000, quote=False, ragged=True, seed=6)
+    assert int(lens.min()) >= 0 and int(lens.max()) <= 40 and len(set(lens.tolist())) > 10

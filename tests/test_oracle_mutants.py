@@ -213,3 +213,35 @@ def test_accept_counts_matches_not_prefix_mutant_is_caught(monkeypatch):
         except AssertionError:
             failed += 1
     assert failed >= 1
+
+
+def _context_mutant(kind):
+    from numpy.lib.stride_tricks import sliding_window_view
+
+    def row(context, n_max, n_min, K):
+        c = np.asarray(context).astype(np.int64)
+        L = c.shape[0]
+        order = range(n_min, n_max + 1) if kind == "shortest_first" else range(n_max, n_min - 1, -1)
+        for n in order:
+            if L - 1 < n:
+                continue
+            pattern = c[L - n:]
+            hay = c if kind == "pattern_matches_itself" else c[:L - 1]
+            win = sliding_window_view(hay, n)
+            hits = np.flatnonzero((win == pattern).all(axis=1))
+            if hits.size:
+                j = int(hits[0] if kind == "earliest" else hits[-1])
+                e = j + (n + 1 if kind == "skip_one" else (0 if kind == "copy_pattern" else n))
+                return c[e:e + K].tolist(), n, e
+        return [], 0, -1
+    return row
+
+
+@pytest.mark.parametrize("kind", ["shortest_first", "pattern_matches_itself", "earliest",
+                                  "skip_one", "copy_pattern"])
+def test_context_drafts_mutant_is_caught(kind, monkeypatch):
+    from oracle import context_lookup as ctx_mod
+    monkeypatch.setattr(ctx_mod, "context_drafts_row", _context_mutant(kind))
+    monkeypatch.setattr(oracle, "context_drafts_row", _context_mutant(kind))
+    with pytest.raises(AssertionError):
+        pins.test_context_drafts_handworked_golden()

@@ -407,3 +407,66 @@ def test_accept_all_equal_rows_pick_index_zero():
     logits = np.full((2, 3, 17), 0.125)
     tgt, a = oracle.accept_greedy(logits, np.zeros((2, 3), dtype=np.int32))
     assert (tgt == 0).all() and (a == 3).all()
+
+
+# ----------------------------------------------------------------------------- context drafts
+
+def _parse_context_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "handworked_context_drafts.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("->", 1)
+            parts = lhs.split()
+            toks = [int(x) for x in parts[1:] if "=" not in x and x != "-"]
+            kv = dict(p.split("=") for p in parts if "=" in p)
+            out = dict(p.split("=") for p in rhs.split())
+            drafts = [] if out["drafts"] == "-" else [int(x) for x in out["drafts"].split(",")]
+            cases.append((toks, int(kv["nmax"]), int(kv["nmin"]), int(kv["K"]), drafts, int(out["n"])))
+    return cases
+
+
+def test_context_drafts_handworked_golden():
+    for toks, n_max, n_min, K, want, n in _parse_context_golden():
+        d, got_n, _ = oracle.context_drafts_row(toks, n_max, n_min, K)
+        assert (d, got_n) == (want, n), toks
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_context_drafts_against_string_rfind(seed):
+    # brute force by an independent route: with one character per token, the latest
+    # occurrence of the last n tokens that ends before the last token is str.rfind of the
+    # pattern in the context without its last token
+    rng = np.random.default_rng(900 + seed)
+    for _ in range(400):
+        L = int(rng.integers(0, 30))
+        toks = rng.integers(0, 3 + seed, L).tolist()
+        n_max = int(rng.integers(1, 6))
+        n_min = int(rng.integers(1, n_max + 1))
+        K = int(rng.integers(1, 9))
+        s = "".join(chr(97 + t) for t in toks)
+        want, want_n = [], 0
+        for n in range(n_max, n_min - 1, -1):
+            if n > L - 1:
+                continue
+            j = s[:L - 1].rfind(s[L - n:])
+            if j >= 0:
+                want, want_n = toks[j + n:j + n + K], n
+                break
+        d, n, e = oracle.context_drafts_row(toks, n_max, n_min, K)
+        assert (d, n) == (want, want_n), (toks, n_max, n_min, K)
+        if n:
+            assert toks[e - n:e] == toks[L - n:] and len(d) == min(K, L - e)
+
+
+def test_context_drafts_batch_pads_and_uses_lengths():
+    ctx = np.array([[1, 2, 3, 1, 2, 99, 99],
+                    [6, 6, 6, 0, 0, 0, 0],
+                    [4, 5, 4, 5, 4, 5, 4]])
+    d, c, m = oracle.context_drafts(ctx, [5, 3, 7], 3, 1, 4)
+    assert d[0].tolist() == [3, 1, 2, -1] and c[0] == 3 and m[0] == 2
+    assert d[1].tolist() == [6, -1, -1, -1] and c[1] == 1 and m[1] == 2
+    # latest occurrence of 4 5 4 ending before the last token starts at 2: drafts = 5 4
+    assert d[2].tolist() == [5, 4, -1, -1] and c[2] == 2 and m[2] == 3

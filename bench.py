@@ -430,6 +430,52 @@ def batch_row(device, stream, steps=10, warmup=3):
     return res
 
 
+def context_bytes(lengths, K):
+    """Algorithmic bytes of one dn_context_drafts launch: every context token read once,
+    plus the length read and the drafts, count and match length written per request."""
+    return 4 * int(sum(int(x) for x in lengths)) + len(lengths) * 4 * (1 + K + 2)
+
+
+def context_row(device, stream, launches=200, warmup=5):
+    """Drafting from the request's own context, once per verify step: the single-user
+    document-reproduction case (25,000-token prompt + 1,000 quoted tokens) and 64 requests
+    at a 268,000-token context (4 rotating sets, 274 MB, larger than L2)."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300 import inputs
+    out = {}
+    for name, N, prompt, gen, nsets in [("single_user_p25000_g1000", 1, 25000, 1000, 3),
+                                        ("batch64_p268000_g500", 64, 268000, 500, 4)]:
+        sets = []
+        for i in range(nsets):
+            ctx, lens = inputs.context_inputs(N, prompt, gen, 151936, quote=True, seed=1100 + i)
+            sets.append((ctx.to(device), lens.to(device),
+                         torch.empty((N, 8), dtype=torch.int32, device=device),
+                         torch.empty((N,), dtype=torch.int32, device=device),
+                         torch.empty((N,), dtype=torch.int32, device=device)))
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                c = sets[i % nsets]
+                dn.dn_context_drafts(c[0], c[1], 4, 1, 8, c[2], c[3], c[4], stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(launches)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(launches):
+                c = sets[i % nsets]
+                evs[i][0].record(stream)
+                dn.dn_context_drafts(c[0], c[1], 4, 1, 8, c[2], c[3], c[4], stream=stream)
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        nbytes = context_bytes(sets[0][1].tolist(), 8)
+        found = int(sets[(launches - 1) % nsets][3].min())
+        out[name] = {"us_per_lookup": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
+                     "bytes": nbytes, "drafts_found_min": found, "n_max": 4, "K": 8}
+        del sets
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_inputs(w, heads, seed):
@@ -561,6 +607,7 @@ def main():
         rows["recompute_on_commit_step"] = deltas_row(sets, device, stream)
         rows["batch64_step"] = batch_row(device, stream)
         rows["prefill"] = prefill_row(device, stream)
+        rows["context_drafts"] = context_row(device, stream)
     clocks.stop()
     gpu_index = local
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")

@@ -41,6 +41,7 @@ SIGNATURES = {
     "dn_prefix_cache_insert": (_I, [_P, _P, _I, ctypes.c_int32, _P]),
     "dn_prefix_cache_lookup": (_I, [_P, _P, _I, _P, _P]),
     "dn_prefix_cache_size": (_I, [_P]),
+    "dn_context_drafts": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -232,6 +233,30 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
 
 def dn_prefill_wait_timeouts():
     return int(load_library().dn_prefill_wait_timeouts())
+
+
+def dn_context_drafts(context, lengths, n_max=4, n_min=1, K=8, drafts=None, count=None,
+                      match_len=None, stream=None):
+    """Drafts copied from each request's context: context [N, stride] int32, lengths [N] int32.
+
+    Returns (drafts [N, K] int32 padded with -1, count [N] int32, match_len [N] int32).
+    """
+    N, stride = context.shape
+    dev = context.device
+    if drafts is None:
+        drafts = torch.empty((N, K), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty((N,), dtype=torch.int32, device=dev)
+    if match_len is None:
+        match_len = torch.empty((N,), dtype=torch.int32, device=dev)
+    _dev(context, lengths, drafts, count, match_len)
+    assert context.dtype == lengths.dtype == drafts.dtype == count.dtype == torch.int32
+    assert lengths.shape == (N,) and drafts.shape == (N, K) and count.shape == (N,)
+    st = load_library().dn_context_drafts(N, stride, n_max, n_min, K, _ptr(context), _ptr(lengths),
+                                          _ptr(drafts), _ptr(count), _ptr(match_len),
+                                          _stream(stream))
+    _check("dn_context_drafts", st)
+    return drafts, count, match_len
 
 
 class PrefixCache:

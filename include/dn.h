@@ -273,6 +273,37 @@ dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logit_dt, const
                                    int32_t *accepted_len, dn_stream_t stream);
 
 /*
+ * dn_context_drafts -- draft tokens copied from each request's own context.
+ *
+ * Single-user serving fills the later positions of the verify block (after the drafter's
+ * 7) by copying from the request's context, since models often quote their input verbatim
+ * ([P1]; [P4]: on document reproduction about 15 of 16 block tokens are accepted). The
+ * pages do not say how the place to copy from is found; the rule here: the pattern is the
+ * last n tokens of the context; take its latest earlier occurrence that has at least one
+ * token after it, for the largest n in n_min..n_max that has one; the drafts are the up to
+ * K tokens that follow it. No occurrence for any n: no drafts.
+ *
+ *   N          requests, >= 0
+ *   stride     row pitch of context in tokens, 0 .. 2^27 - 1
+ *   n_max      1 .. DN_MAX_NGRAM;  n_min  1 .. n_max
+ *   K          drafts wanted, 1 .. DN_MAX_BLOCK
+ *   context    [N][stride] int32 token ids (device); row r is prompt then generated tokens
+ *   lengths    [N] int32 (device): row r uses context[r][0 .. lengths[r]); a length
+ *              below 0 counts as 0 and one above stride as stride
+ *   drafts     [N][K] int32 (device, written): the drafts, then -1 up to K
+ *   count      [N] int32 (device, written): drafts found, 0 .. K
+ *   match_len  [N] int32 (device, written) or NULL: the n used, 0 if none
+ *
+ * Reads L * 4 bytes per request; lengths are read on the device, so a caller that appends
+ * accepted tokens on the device needs no host round trip. All pointers 4-byte aligned.
+ * Returns DN_ERR_INVALID_ARG for bad sizes or pointers, DN_ERR_CUDA if the launch fails.
+ */
+#define DN_MAX_NGRAM 16
+dn_status dn_context_drafts(int N, int stride, int n_max, int n_min, int K, const int32_t *context,
+                            const int32_t *lengths, int32_t *drafts, int32_t *count,
+                            int32_t *match_len, dn_stream_t stream);
+
+/*
  * Prefix index for recurrent-state checkpoints (host memory, no GPU work).
  *
  * Prefix caching keeps the DeltaNet state so that a later turn restores it instead of

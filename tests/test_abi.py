@@ -178,3 +178,31 @@ def test_binding_raises_dnerror_on_bad_status(lib):
 def test_binding_refuses_missing_library(tmp_path):
     with pytest.raises(RuntimeError):
         binding.load_library(str(tmp_path / "missing.so"))
+
+
+def _context_args(buf, **over):
+    a = dict(N=2, stride=100, n_max=4, n_min=1, K=8, ctx=buf(800), lens=buf(), drafts=buf(64),
+             count=buf(), match=None)
+    a.update(over)
+    return (a["N"], a["stride"], a["n_max"], a["n_min"], a["K"], a["ctx"], a["lens"], a["drafts"],
+            a["count"], a["match"], None)
+
+
+@pytest.mark.parametrize("over", [
+    dict(N=-1), dict(stride=-1), dict(stride=1 << 27), dict(n_min=0), dict(n_min=5),
+    dict(n_max=17, n_min=1), dict(K=0), dict(K=17), dict(ctx=None), dict(lens=None),
+    dict(drafts=None), dict(count=None), "misaligned_ctx", "misaligned_match",
+])
+def test_context_drafts_rejects(lib, over):
+    buf = Bufs()
+    if over == "misaligned_ctx":
+        over = dict(ctx=buf(offset=2))
+    elif over == "misaligned_match":
+        over = dict(match=buf(offset=1))
+    assert lib.dn_context_drafts(*_context_args(buf, **over)) == INVALID
+
+
+def test_context_drafts_empty_is_ok(lib):
+    buf = Bufs()
+    assert lib.dn_context_drafts(*_context_args(buf, N=0, ctx=None, lens=None, drafts=None,
+                                                count=None)) == OK

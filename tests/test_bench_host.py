@@ -93,3 +93,9 @@ def test_clock_sampler_summary_parsing():
 
 def test_kernel_sources_hash_is_stable():
     assert bench.kernel_sources_hash() == bench.kernel_sources_hash()
+
+
+def test_context_bytes():
+    # every token once, plus length in and (drafts, count, match length) out per request
+    assert bench.context_bytes([26000], 8) == 26000 * 4 + 4 * (1 + 8 + 2)
+    assert bench.context_bytes([10, 0], 4) == 40 + 2 * 4 * 7

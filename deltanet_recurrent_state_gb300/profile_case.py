@@ -4,6 +4,7 @@
     python -m deltanet_recurrent_state_gb300.profile_case accept  [--requests 128]
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
     python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1]
+    python -m deltanet_recurrent_state_gb300.profile_case context [--tokens 268000] [--requests 64]
 
 Shapes are those of the single-user workload (48 heads, 128 x 128 fp16 state,
 T = 16) with fewer layers, sized so the footprint stays a few hundred MB but
@@ -24,7 +25,7 @@ from deltanet_recurrent_state_gb300 import inputs  # noqa: E402
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["verify", "accept", "commit", "prefill"])
+    ap.add_argument("kernel", choices=["verify", "accept", "commit", "prefill", "context"])
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--requests", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=4096)
@@ -50,6 +51,11 @@ def main():
         ws = dn.accept_workspace(B, T4, V, dev)
         for _ in range(a.warmup + a.launches):
             dn.dn_accept_greedy(logits, draft, workspace=ws)
+    elif a.kernel == "context":
+        ctx, lens = inputs.context_inputs(a.requests, a.tokens, 500, V, quote=True, seed=5)
+        ctx, lens = ctx.to(dev), lens.to(dev)
+        for _ in range(a.warmup + a.launches):
+            dn.dn_context_drafts(ctx, lens, 4, 1, 8)
     else:
         x = inputs.recurrence_inputs(a.sequences, a.tokens, H, d, d, seed=4, device=dev)
         for _ in range(a.warmup + a.launches):

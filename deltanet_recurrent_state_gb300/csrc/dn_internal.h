@@ -26,4 +26,9 @@ inline dn_status launch_status() {
     return cudaGetLastError() == cudaSuccess ? DN_OK : DN_ERR_CUDA;
 }
 
+// Chunkwise fp16 prefill on tcgen05 tensor cores for dk = dv = 128 (dn_prefill_tc.cu).
+dn_status launch_prefill_tc(int N, int H, int P, const void *q, const void *k, const void *v, const float *beta,
+                            const float *g, const void *s_in, void *out, void *ckpt, void *s_out, cudaStream_t st);
+unsigned int prefill_tc_wait_timeouts();
+
 }  // namespace dn

@@ -27,6 +27,7 @@
 #include "dn_internal.h"
 #include "dn_mma.cuh"
 #include "dn_recurrence.cuh"
+#include "dn_tmap.h"
 
 namespace dn {
 namespace {
@@ -534,34 +535,6 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
 }
 
-// cuTensorMapEncodeTiled from the driver (no link-time dependency on libcuda).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    }
-    return fn;
-}
-
-// fp16 tensor map over `rank` dims (innermost first), 64-column boxes, 128-byte swizzle.
-bool encode_map(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-                const cuuint64_t *strides_bytes, const cuuint32_t *box) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-               strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -646,7 +619,8 @@ extern "C" unsigned int dn_prefill_wait_timeouts(void) {
         cudaGetLastError();
         return 0xffffffffu;
     }
-    return v;
+    const unsigned int w = dn::prefill_tc_wait_timeouts();
+    return w == 0xffffffffu ? w : v + w;
 }
 
 extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int dk, int dv,
@@ -671,7 +645,7 @@ extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int d
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (io_dt == DN_F16) {
         dn_status r;
-        if (dk == 128 && dv == 128) r = launch_prefill_wy<128, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        if (dk == 128 && dv == 128) r = launch_prefill_tc(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else if (dk == 128) r = launch_prefill_wy<128, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else if (dv == 128) r = launch_prefill_wy<64, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else r = launch_prefill_wy<64, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);

@@ -31,6 +31,8 @@ SIGNATURES = {
     "dn_commit": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "dn_prefill_checkpoint": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P]),
+    "dn_prefill_checkpoint_tc": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                      _P, _P, _P]),
     "dn_status_string": (ctypes.c_char_p, [_I]),
     "dn_accept_greedy_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dn_prefill_wait_timeouts": (ctypes.c_uint, []),
@@ -204,10 +206,11 @@ def dn_commit(ckpt, accepted_len, state, stream=None):
 
 
 def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, state_out=None,
-                          chunk=PREFILL_CHUNK, state_dtype=None, stream=None):
+                          chunk=PREFILL_CHUNK, state_dtype=None, stream=None, engine="mma"):
     """q, k [N,P,H,dk]; v [N,P,H,dv]; beta, g [N,P,H]; state_in [N,H,dv,dk] or None.
 
     Returns (out [N,P,H,dv], ckpt [N,P//chunk,H,dv,dk], state_out [N,H,dv,dk]).
+    engine "mma" calls dn_prefill_checkpoint, "tc" dn_prefill_checkpoint_tc (fp16, 128 x 128).
     """
     N, P, H, dk = q.shape
     dv = v.shape[-1]
@@ -223,11 +226,12 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
     assert k.shape == q.shape and v.shape == (N, P, H, dv) and beta.shape == (N, P, H)
     assert g.shape == (N, P, H) and out.shape == (N, P, H, dv)
     assert ckpt.shape == (N, P // chunk, H, dv, dk) and state_out.shape == (N, H, dv, dk)
-    st = load_library().dn_prefill_checkpoint(
+    name = {"mma": "dn_prefill_checkpoint", "tc": "dn_prefill_checkpoint_tc"}[engine]
+    st = getattr(load_library(), name)(
         N, H, P, chunk, dk, dv, _DT[q.dtype], _DT[sdt], _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
         _ptr(g), _ptr(state_in), _ptr(out), _ptr(ckpt) if ckpt.numel() else None,
         _ptr(state_out), _stream(stream))
-    _check("dn_prefill_checkpoint", st)
+    _check(name, st)
     return out, ckpt, state_out
 
 

@@ -645,7 +645,7 @@ extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int d
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (io_dt == DN_F16) {
         dn_status r;
-        if (dk == 128 && dv == 128) r = launch_prefill_tc(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
+        if (dk == 128 && dv == 128) r = launch_prefill_wy<128, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else if (dk == 128) r = launch_prefill_wy<128, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else if (dv == 128) r = launch_prefill_wy<64, 128>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else r = launch_prefill_wy<64, 64>(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
@@ -654,5 +654,28 @@ extern "C" dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int d
         if (dk == 128) launch_prefill_seq<128, float, float>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
         else launch_prefill_seq<64, float, float>(N, H, P, chunk, dv, q, k, v, beta, g, state_in, out, ckpt, state_out, st);
     }
+    return launch_status();
+}
+
+extern "C" dn_status dn_prefill_checkpoint_tc(int N, int H, int P, int chunk, int dk, int dv, dn_dtype io_dt,
+                                              dn_dtype state_dt, const void *q, const void *k, const void *v,
+                                              const float *beta, const float *g, const void *state_in, void *out,
+                                              void *ckpt, void *state_out, dn_stream_t stream) {
+    using namespace dn;
+    if (N < 0 || H < 1 || P < 0) return DN_ERR_INVALID_ARG;
+    if (!dtype_ok(io_dt) || !dtype_ok(state_dt)) return DN_ERR_INVALID_ARG;
+    if (chunk != DN_PREFILL_CHUNK) return DN_ERR_UNSUPPORTED;
+    if (dk != 128 || dv != 128 || io_dt != DN_F16 || state_dt != DN_F16) return DN_ERR_UNSUPPORTED;
+    if (N == 0) return DN_OK;
+    if (!state_out) return DN_ERR_INVALID_ARG;
+    if (P > 0 && (!q || !k || !v || !beta || !g || !out)) return DN_ERR_INVALID_ARG;
+    if (P >= chunk && !ckpt) return DN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(ckpt, 16) ||
+        !aligned(state_in, 16) || !aligned(state_out, 16) || !aligned(beta, 4) || !aligned(g, 4))
+        return DN_ERR_INVALID_ARG;
+    if ((long long)N * H > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
+    const dn_status r = launch_prefill_tc(N, H, P, q, k, v, beta, g, state_in, out, ckpt, state_out,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    if (r != DN_OK) return r;
     return launch_status();
 }

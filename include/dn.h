@@ -241,6 +241,24 @@ dn_status dn_prefill_checkpoint(int N, int H, int P, int chunk, int dk, int dv,
                                 void *state_out, dn_stream_t stream);
 
 /*
+ * dn_prefill_checkpoint_tc -- dn_prefill_checkpoint on the fifth-generation tensor cores.
+ *
+ * Same operation, arguments, layouts, ownership and errors as dn_prefill_checkpoint, for
+ * fp16 io and state with dk = dv = 128 only (DN_ERR_UNSUPPORTED otherwise). The chunk is
+ * computed in its 64-token form: grams, the WY factors U and W and the per-chunk state
+ * products are tcgen05 MMAs with accumulators in tensor memory; the 64 x 64 triangular
+ * inverse is solved in 16 x 16 blocks. Results agree with the oracle within the fp16
+ * tolerance and restores from its checkpoints are bit-identical, but the rounding order
+ * differs from dn_prefill_checkpoint, so the two engines' outputs are not bit-identical
+ * to each other. On GB300 it is slower than dn_prefill_checkpoint on the 25,000-token
+ * workload (the per-chunk chain of dependent steps, not the tensor pipe, bounds it).
+ */
+dn_status dn_prefill_checkpoint_tc(int N, int H, int P, int chunk, int dk, int dv, dn_dtype io_dt,
+                                   dn_dtype state_dt, const void *q, const void *k, const void *v,
+                                   const float *beta, const float *g, const void *state_in, void *out,
+                                   void *ckpt, void *state_out, dn_stream_t stream);
+
+/*
  * dn_accept_greedy_noalloc -- dn_accept_greedy without a caller-supplied workspace.
  *
  * The pages have no counterpart to this entry point; it exists for callers that

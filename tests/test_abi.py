@@ -206,3 +206,17 @@ def test_context_drafts_empty_is_ok(lib):
     buf = Bufs()
     assert lib.dn_context_drafts(*_context_args(buf, N=0, ctx=None, lens=None, drafts=None,
                                                 count=None)) == OK
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(dk=64), UNSUPPORTED), (dict(io=F32, st=F32), UNSUPPORTED), (dict(P=-1), INVALID),
+    (dict(s_out=None), INVALID), ("misaligned_out", INVALID),
+])
+def test_prefill_tc_rejects(lib, over, want):
+    buf = Bufs()
+    base = dict(dk=128, dv=128, io=F16, st=F16, q=buf(70 * 256), k=buf(70 * 256), v=buf(70 * 256),
+                out=buf(70 * 256), ckpt=buf(128 * 128 * 2), s_out=buf(128 * 128 * 2))
+    if over == "misaligned_out":
+        over = dict(out=buf(offset=4))
+    base.update(over)
+    assert lib.dn_prefill_checkpoint_tc(*_prefill_args(buf, **base)) == want

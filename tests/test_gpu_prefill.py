@@ -123,3 +123,53 @@ def test_whole_and_half_row_ctas_agree(cuda):
     assert_close("out", o_all[:1, :, heads], ref[0], TOL["f16"])
     assert_close("ckpt", c_all[:1, :, heads], ref[1], TOL["f16"])
     assert_close("state_out", s_all[:1, heads], ref[2], TOL["f16"])
+
+
+# ---------------------------------------------------------------------------- tcgen05 engine
+
+@pytest.mark.parametrize("P", [0, 1, 15, 63, 64, 65, 129, 200])
+def test_tc_engine_against_oracle(P, cuda):
+    x = inputs.recurrence_inputs(2, P, 3, 128, 128, io="f16", state="f16", seed=700 + P, device="cpu")
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k].to(cuda) for k in KEYS], x["state"].to(cuda), engine="tc")
+    torch.cuda.synchronize()
+    ref = oracle.prefill_checkpoint(*[np64(x[k]) for k in KEYS], np64(x["state"]), chunk=64, store="f16", io="f16")
+    assert_close("out", out, ref[0], TOL["f16"])
+    assert_close("ckpt", ckpt, ref[1], TOL["f16"])
+    assert_close("state_out", s_out, ref[2], TOL["f16"])
+
+
+def test_tc_engine_no_initial_state_and_restore(cuda):
+    N, P, H, d = 1, 300, 4, 128
+    x = inputs.recurrence_inputs(N, P, H, d, d, seed=701, device=cuda)
+    args = [x[k] for k in KEYS]
+    o0, c0, s0 = dn.dn_prefill_checkpoint(*args, None, state_dtype=torch.float16, engine="tc")
+    ref = oracle.prefill_checkpoint(*[np64(a) for a in args], None, chunk=64, store="f16", io="f16")
+    assert_close("state_out", s0, ref[2], TOL["f16"])
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*args, x["state"], engine="tc")
+    for c in range(P // 64):
+        start = 64 * (c + 1)
+        tail = [a[:, start:].contiguous() for a in args]
+        o2, ck2, s2 = dn.dn_prefill_checkpoint(*tail, ckpt[:, c].contiguous(), engine="tc")
+        torch.cuda.synchronize()
+        assert torch.equal(s2, s_out) and torch.equal(o2, out[:, start:]) and torch.equal(ck2, ckpt[:, c + 1:])
+
+
+def test_tc_engine_rejects_other_shapes(cuda):
+    x = inputs.recurrence_inputs(1, 64, 2, 64, 128, seed=702, device=cuda)
+    with pytest.raises(dn.DnError):
+        dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"], engine="tc")
+
+
+def test_tc_engine_full_size_layer_sampled(cuda):
+    # one 25,000-token layer (48 heads); sampled heads against the oracle
+    x = inputs.recurrence_inputs(1, 25000, 48, 128, 128, seed=703, device=cuda)
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"], engine="tc")
+    torch.cuda.synchronize()
+    assert dn.dn_prefill_wait_timeouts() == 0
+    heads = [0, 29, 47]
+    u = {k: np64(x[k][:, :, heads]) for k in KEYS}
+    ref = oracle.prefill_checkpoint(u["q"], u["k"], u["v"], u["beta"], u["g"], np64(x["state"][:, heads]),
+                                    chunk=64, store="f16", io="f16")
+    assert_close("out", out[:, :, heads], ref[0], TOL["f16"])
+    assert_close("ckpt", ckpt[:, :, heads], ref[1], TOL["f16"])
+    assert_close("state_out", s_out[:, heads], ref[2], TOL["f16"])

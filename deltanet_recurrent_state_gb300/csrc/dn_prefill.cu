@@ -207,6 +207,10 @@ __device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
 constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6;
 constexpr int kPrepThreads = 128;
 constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
+// 16-row state tiles per chain warp. Two tiles per warp halve the operand fragments each
+// warp loads from shared memory but measure no faster on GB300 (the chain is bound by the
+// latency of its dependent steps, not by shared-memory bandwidth), so one it is.
+constexpr int kRowTiles = 1;
 
 // Count of prefill input waits that ran out (read by dn_prefill_wait_timeouts).
 __device__ unsigned int g_prefill_wait_timeouts;
@@ -215,14 +219,14 @@ struct PrefillMaps {
     CUtensorMap q, k, v, o, ck;
 };
 
-template <int DK, int DV, int DVC>
-__global__ void __launch_bounds__(DVC * 2 + kPrepThreads, 1)
+template <int DK, int DV, int DVC, int RT>
+__global__ void __launch_bounds__(DVC * 2 / RT + kPrepThreads, 1)
 prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                   const float *__restrict__ beta, const float *__restrict__ g,
                   const __half *s_in, __half *s_out) {
     using L = PrefillSmem<DK, DVC>;
     constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
-    constexpr int NW = DVC / 16, NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
+    constexpr int NW = DVC / (16 * RT), NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
     constexpr int BOXU = C * 8;   // uint4 per 64 x 64 box
@@ -373,19 +377,24 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
 
     // ============================== chain warps ==============================
-    const int i0 = warp * 16;  // this warp's rows within the CTA (state rows r0 + i0 ..)
-    float DS[NTK][4];          // state tile nt: dk columns 8nt .. 8nt+7 of rows i0 .. i0+15
+    // A chain warp owns RT 16-row tiles of the state (rows i0 .. i0 + 16 RT - 1); every
+    // operand fragment it loads from shared memory for the projections and the state
+    // update serves all RT tiles.
+    const int i0 = warp * 16 * RT;  // this warp's rows within the CTA (state rows r0 + i0 ..)
+    float DS[RT][NTK][4];           // tile mt, nt: rows i0 + 16 mt .., dk columns 8nt .. 8nt+7
 #pragma unroll
-    for (int nt = 0; nt < NTK; ++nt) {
-        float2 lo = make_float2(0.f, 0.f), hi = lo;
-        if (s_in) {
-            lo = __half22float2(*reinterpret_cast<const __half2 *>(
-                s_in + state_off + (size_t)(r0 + i0 + fr) * DK + 8 * nt + fc));
-            hi = __half22float2(*reinterpret_cast<const __half2 *>(
-                s_in + state_off + (size_t)(r0 + i0 + fr + 8) * DK + 8 * nt + fc));
+    for (int mt = 0; mt < RT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NTK; ++nt) {
+            float2 lo = make_float2(0.f, 0.f), hi = lo;
+            if (s_in) {
+                lo = __half22float2(*reinterpret_cast<const __half2 *>(
+                    s_in + state_off + (size_t)(r0 + i0 + 16 * mt + fr) * DK + 8 * nt + fc));
+                hi = __half22float2(*reinterpret_cast<const __half2 *>(
+                    s_in + state_off + (size_t)(r0 + i0 + 16 * mt + fr + 8) * DK + 8 * nt + fc));
+            }
+            DS[mt][nt][0] = lo.x; DS[mt][nt][1] = lo.y; DS[mt][nt][2] = hi.x; DS[mt][nt][3] = hi.y;
         }
-        DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
-    }
 
     for (int c = 0; c < nchunks; ++c) {
         const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3, ob = c & 1;
@@ -399,12 +408,11 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
 #pragma unroll 1
         for (int j = 0; j < NSUB; ++j) {
             if (16 * j >= nc) break;
-            unsigned aS[KS][4];
+            float X[RT][4][4];
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) acc_to_a(aS[ks], DS[2 * ks], DS[2 * ks + 1]);
-            float X[4][4];
+            for (int mt = 0; mt < RT; ++mt)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) X[u][0] = X[u][1] = X[u][2] = X[u][3] = 0.f;
+                for (int u = 0; u < 4; ++u) X[mt][u][0] = X[mt][u][1] = X[mt][u][2] = X[mt][u][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {  // X = S [K_j;Q_j]^T
                 unsigned bk[4], bq[4];
@@ -414,54 +422,62 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 ldsm_x4(bq, cQ + box_chunk(C, r, cc));
                 const unsigned k0[2] = {bk[0], bk[1]}, k1[2] = {bk[2], bk[3]};
                 const unsigned q0[2] = {bq[0], bq[1]}, q1[2] = {bq[2], bq[3]};
-                mma_16816(X[0], aS[ks], k0);
-                mma_16816(X[1], aS[ks], k1);
-                mma_16816(X[2], aS[ks], q0);
-                mma_16816(X[3], aS[ks], q1);
-            }
-            unsigned vt[4];
-            ldsm_x4_t(vt, cV + box_chunk(C, 16 * j + ((lane >> 4) << 3) + (lane & 7),
-                                         (i0 >> 3) + ((lane >> 3) & 1)));
-            float R[2][4], Dl[2][4], O[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {  // R = V^T - gam X_K ; O starts at gam X_Q
-                const int t = 16 * j + 8 * nt + fc;
-                const float ga = gam[t], gb = gam[t + 1];
-                const float2 lo = unpack_h2(vt[2 * nt]), hi = unpack_h2(vt[2 * nt + 1]);
-                R[nt][0] = lo.x - ga * X[nt][0];
-                R[nt][1] = lo.y - gb * X[nt][1];
-                R[nt][2] = hi.x - ga * X[nt][2];
-                R[nt][3] = hi.y - gb * X[nt][3];
-                O[nt][0] = ga * X[2 + nt][0];
-                O[nt][1] = gb * X[2 + nt][1];
-                O[nt][2] = ga * X[2 + nt][2];
-                O[nt][3] = gb * X[2 + nt][3];
-                Dl[nt][0] = Dl[nt][1] = Dl[nt][2] = Dl[nt][3] = 0.f;
+                for (int mt = 0; mt < RT; ++mt) {
+                    unsigned aS[4];
+                    acc_to_a(aS, DS[mt][2 * ks], DS[mt][2 * ks + 1]);
+                    mma_16816(X[mt][0], aS, k0);
+                    mma_16816(X[mt][1], aS, k1);
+                    mma_16816(X[mt][2], aS, q0);
+                    mma_16816(X[mt][3], aS, q1);
+                }
             }
-            {   // Delta^T = R Tb^T
-                unsigned aR[4], bt[4];
-                acc_to_a(aR, R[0], R[1]);
-                ldsm_x4(bt, &sTb[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
-                const unsigned t0[2] = {bt[0], bt[1]}, t1[2] = {bt[2], bt[3]};
-                mma_16816(Dl[0], aR, t0);
-                mma_16816(Dl[1], aR, t1);
-            }
-            {   // O^T += Delta^T Mq^T
-                unsigned aD[4], bm[4];
-                acc_to_a(aD, Dl[0], Dl[1]);
-                ldsm_x4(bm, &sMq[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
-                const unsigned m0[2] = {bm[0], bm[1]}, m1[2] = {bm[2], bm[3]};
-                mma_16816(O[0], aD, m0);
-                mma_16816(O[1], aD, m1);
-            }
-            {   // O^T tile -> O box rows t (token), columns i (dv)
-                const int m = lane >> 3, t = 16 * j + 8 * (m >> 1) + (lane & 7);
-                stsm_x4_t(cO + box_chunk(C, t, (i0 >> 3) + (m & 1)),
-                          pack_h2(O[0][0], O[0][1]), pack_h2(O[0][2], O[0][3]),
-                          pack_h2(O[1][0], O[1][1]), pack_h2(O[1][2], O[1][3]));
-            }
-            {   // S = gam_15 S + (Delta^T diag(e^{G_15 - G})) K_j
-                float Dt[2][4];
+            unsigned bt[4], bm[4];
+            ldsm_x4(bt, &sTb[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+            ldsm_x4(bm, &sMq[pb][j][(lane & 7) + ((lane >> 4) << 3)][8 * ((lane >> 3) & 1)]);
+            const unsigned t0[2] = {bt[0], bt[1]}, t1[2] = {bt[2], bt[3]};
+            const unsigned m0[2] = {bm[0], bm[1]}, m1[2] = {bm[2], bm[3]};
+            unsigned aT[RT][4];
+#pragma unroll
+            for (int mt = 0; mt < RT; ++mt) {
+                const int im = i0 + 16 * mt;
+                unsigned vt[4];
+                ldsm_x4_t(vt, cV + box_chunk(C, 16 * j + ((lane >> 4) << 3) + (lane & 7), (im >> 3) + ((lane >> 3) & 1)));
+                float R[2][4], Dl[2][4], O[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {  // R = V^T - gam X_K ; O starts at gam X_Q
+                    const int t = 16 * j + 8 * nt + fc;
+                    const float ga = gam[t], gb = gam[t + 1];
+                    const float2 lo = unpack_h2(vt[2 * nt]), hi = unpack_h2(vt[2 * nt + 1]);
+                    R[nt][0] = lo.x - ga * X[mt][nt][0];
+                    R[nt][1] = lo.y - gb * X[mt][nt][1];
+                    R[nt][2] = hi.x - ga * X[mt][nt][2];
+                    R[nt][3] = hi.y - gb * X[mt][nt][3];
+                    O[nt][0] = ga * X[mt][2 + nt][0];
+                    O[nt][1] = gb * X[mt][2 + nt][1];
+                    O[nt][2] = ga * X[mt][2 + nt][2];
+                    O[nt][3] = gb * X[mt][2 + nt][3];
+                    Dl[nt][0] = Dl[nt][1] = Dl[nt][2] = Dl[nt][3] = 0.f;
+                }
+                {   // Delta^T = R Tb^T
+                    unsigned aR[4];
+                    acc_to_a(aR, R[0], R[1]);
+                    mma_16816(Dl[0], aR, t0);
+                    mma_16816(Dl[1], aR, t1);
+                }
+                {   // O^T += Delta^T Mq^T
+                    unsigned aD[4];
+                    acc_to_a(aD, Dl[0], Dl[1]);
+                    mma_16816(O[0], aD, m0);
+                    mma_16816(O[1], aD, m1);
+                }
+                {   // O^T tile -> O box rows t (token), columns i (dv)
+                    const int m = lane >> 3, t = 16 * j + 8 * (m >> 1) + (lane & 7);
+                    stsm_x4_t(cO + box_chunk(C, t, (im >> 3) + (m & 1)),
+                              pack_h2(O[0][0], O[0][1]), pack_h2(O[0][2], O[0][3]),
+                              pack_h2(O[1][0], O[1][1]), pack_h2(O[1][2], O[1][3]));
+                }
+                float Dt[2][4];  // Delta^T diag(e^{G_15 - G}) as the A operand of the state update
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int t = 16 * j + 8 * nt + fc;
@@ -471,24 +487,30 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                     Dt[nt][2] = Dl[nt][2] * da;
                     Dt[nt][3] = Dl[nt][3] * db;
                 }
-                unsigned aT[4];
-                acc_to_a(aT, Dt[0], Dt[1]);
+                acc_to_a(aT[mt], Dt[0], Dt[1]);
+            }
+            {   // S = gam_15 S + (Delta^T diag(e^{G_15 - G})) K_j
                 const float gend = gam[16 * j + 15];
                 const float2 g2 = make_float2(gend, gend);
 #pragma unroll
-                for (int nt = 0; nt < NTK; ++nt) {
-                    const float2 lo = __fmul2_rn(g2, make_float2(DS[nt][0], DS[nt][1]));
-                    const float2 hi = __fmul2_rn(g2, make_float2(DS[nt][2], DS[nt][3]));
-                    DS[nt][0] = lo.x; DS[nt][1] = lo.y; DS[nt][2] = hi.x; DS[nt][3] = hi.y;
-                }
+                for (int mt = 0; mt < RT; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NTK; ++nt) {
+                        const float2 lo = __fmul2_rn(g2, make_float2(DS[mt][nt][0], DS[mt][nt][1]));
+                        const float2 hi = __fmul2_rn(g2, make_float2(DS[mt][nt][2], DS[mt][nt][3]));
+                        DS[mt][nt][0] = lo.x; DS[mt][nt][1] = lo.y; DS[mt][nt][2] = hi.x; DS[mt][nt][3] = hi.y;
+                    }
 #pragma unroll
                 for (int c2 = 0; c2 < NTK / 2; ++c2) {
                     unsigned bk[4];
                     ldsm_x4_t(bk, cK + box_chunk(C, 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3),
                                                  2 * c2 + (lane >> 4)));
                     const unsigned b0[2] = {bk[0], bk[1]}, b1[2] = {bk[2], bk[3]};
-                    mma_16816(DS[2 * c2], aT, b0);
-                    mma_16816(DS[2 * c2 + 1], aT, b1);
+#pragma unroll
+                    for (int mt = 0; mt < RT; ++mt) {
+                        mma_16816(DS[mt][2 * c2], aT[mt], b0);
+                        mma_16816(DS[mt][2 * c2 + 1], aT[mt], b1);
+                    }
                 }
             }
         }
@@ -498,22 +520,24 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         bar_sync(kBarChain, NTC);
         if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged for the TMA store
 #pragma unroll
-            for (int c2 = 0; c2 < NTK / 2; ++c2) {
-                unsigned r[4];
+            for (int mt = 0; mt < RT; ++mt)
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const __half2 lo = __floats2half2_rn(DS[2 * c2 + u][0], DS[2 * c2 + u][1]);
-                    const __half2 hi = __floats2half2_rn(DS[2 * c2 + u][2], DS[2 * c2 + u][3]);
-                    r[2 * u] = *reinterpret_cast<const unsigned *>(&lo);
-                    r[2 * u + 1] = *reinterpret_cast<const unsigned *>(&hi);
-                    const float2 l2 = __half22float2(lo), h2 = __half22float2(hi);
-                    DS[2 * c2 + u][0] = l2.x; DS[2 * c2 + u][1] = l2.y;
-                    DS[2 * c2 + u][2] = h2.x; DS[2 * c2 + u][3] = h2.y;
+                for (int c2 = 0; c2 < NTK / 2; ++c2) {
+                    unsigned r[4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const __half2 lo = __floats2half2_rn(DS[mt][2 * c2 + u][0], DS[mt][2 * c2 + u][1]);
+                        const __half2 hi = __floats2half2_rn(DS[mt][2 * c2 + u][2], DS[mt][2 * c2 + u][3]);
+                        r[2 * u] = *reinterpret_cast<const unsigned *>(&lo);
+                        r[2 * u + 1] = *reinterpret_cast<const unsigned *>(&hi);
+                        const float2 l2 = __half22float2(lo), h2 = __half22float2(hi);
+                        DS[mt][2 * c2 + u][0] = l2.x; DS[mt][2 * c2 + u][1] = l2.y;
+                        DS[mt][2 * c2 + u][2] = h2.x; DS[mt][2 * c2 + u][3] = h2.y;
+                    }
+                    // matrices: rows 0-7 / 8-15 of dk columns 16c2.., then of 16c2+8..
+                    const int m = lane >> 3, row = i0 + 16 * mt + (m & 1) * 8 + (lane & 7);
+                    stsm_x4(sCk + box_chunk(DVC, row, 2 * c2 + (m >> 1)), r[0], r[1], r[2], r[3]);
                 }
-                // matrices: rows 0-7 / 8-15 of dk columns 16c2.., then of 16c2+8..
-                const int m = lane >> 3, row = i0 + (m & 1) * 8 + (lane & 7);
-                stsm_x4(sCk + box_chunk(DVC, row, 2 * c2 + (m >> 1)), r[0], r[1], r[2], r[3]);
-            }
         }
         fence_proxy_async();
         bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
@@ -527,12 +551,14 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
     if (tid == 0) bulk_wait();
 #pragma unroll
-    for (int nt = 0; nt < NTK; ++nt) {
-        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + fr) * DK + 8 * nt + fc) =
-            __floats2half2_rn(DS[nt][0], DS[nt][1]);
-        *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + fr + 8) * DK + 8 * nt + fc) =
-            __floats2half2_rn(DS[nt][2], DS[nt][3]);
-    }
+    for (int mt = 0; mt < RT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NTK; ++nt) {
+            *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + 16 * mt + fr) * DK + 8 * nt + fc) =
+                __floats2half2_rn(DS[mt][nt][0], DS[mt][nt][1]);
+            *reinterpret_cast<__half2 *>(s_out + state_off + (size_t)(r0 + i0 + 16 * mt + fr + 8) * DK + 8 * nt + fc) =
+                __floats2half2_rn(DS[mt][nt][2], DS[mt][nt][3]);
+        }
 }
 
 int sm_count() {
@@ -545,14 +571,14 @@ int sm_count() {
     return sms;
 }
 
-template <int DK, int DV, int DVC>
+template <int DK, int DV, int DVC, int RT>
 dn_status launch_prefill_wy_split(int N, int H, int P, const void *q, const void *k, const void *v,
                                   const float *beta, const float *g, const void *s_in, void *out,
                                   void *ckpt, void *s_out, cudaStream_t st) {
     constexpr size_t bytes = PrefillSmem<DK, DVC>::kBytes;
     static bool configured = false;  // the attribute is per function and idempotent
     if (!configured) {
-        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, DVC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, DVC, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)bytes) != cudaSuccess) {
             cudaGetLastError();
             return DN_ERR_CUDA;
@@ -581,7 +607,7 @@ dn_status launch_prefill_wy_split(int N, int H, int P, const void *q, const void
         const cuuint32_t box3[3] = {64, (cuuint32_t)DVC, 1};
         if (!encode_map(&maps.ck, ckpt, 3, dims, str, box3)) return DN_ERR_CUDA;
     }
-    prefill_wy_kernel<DK, DV, DVC><<<(unsigned)((long long)N * H * (DV / DVC)), DVC * 2 + kPrepThreads, bytes,
+    prefill_wy_kernel<DK, DV, DVC, RT><<<(unsigned)((long long)N * H * (DV / DVC)), DVC * 2 / RT + kPrepThreads, bytes,
                                       st>>>(
         H, P, maps, beta, g, static_cast<const __half *>(s_in), static_cast<__half *>(s_out));
     return DN_OK;
@@ -592,8 +618,8 @@ dn_status launch_prefill_wy(int N, int H, int P, const void *q, const void *k, c
                             const float *beta, const float *g, const void *s_in, void *out,
                             void *ckpt, void *s_out, cudaStream_t st) {
     if (DV == 128 && (long long)N * H < sm_count())
-        return launch_prefill_wy_split<DK, DV, 64>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
-    return launch_prefill_wy_split<DK, DV, DV>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
+        return launch_prefill_wy_split<DK, DV, 64, kRowTiles>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
+    return launch_prefill_wy_split<DK, DV, DV, kRowTiles>(N, H, P, q, k, v, beta, g, s_in, out, ckpt, s_out, st);
 }
 
 constexpr int kRows = 16;

@@ -20,9 +20,9 @@
 // and stream them through a three-stage shared-memory ring filled by cp.async: two tiles
 // in flight while one is scanned. Each stage also holds the 16 tokens before its tile, so
 // the backward compares after a hit never go to global memory. Each thread turns its 16
-// tokens into a hit mask and walks only the hits. Keys are reduced in shared memory and then into the leader CTA's shared memory
-// with distributed-shared-memory atomics; the leader writes the drafts. HBM bound: L * 4
-// bytes read per request.
+// tokens into a hit mask and walks only the hits. Keys are reduced in shared memory and
+// then into the leader CTA's shared memory with distributed-shared-memory atomics; the
+// leader writes the drafts. HBM bound: L * 4 bytes read per request.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 

@@ -5,6 +5,7 @@
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
     python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1]
     python -m deltanet_recurrent_state_gb300.profile_case context [--tokens 268000] [--requests 64]
+    python -m deltanet_recurrent_state_gb300.profile_case deltas  [--layers 8]
 
 Shapes are those of the single-user workload (48 heads, 128 x 128 fp16 state,
 T = 16) with fewer layers, sized so the footprint stays a few hundred MB but
@@ -25,7 +26,7 @@ from deltanet_recurrent_state_gb300 import inputs  # noqa: E402
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["verify", "accept", "commit", "prefill", "context"])
+    ap.add_argument("kernel", choices=["verify", "accept", "commit", "prefill", "context", "deltas"])
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--requests", type=int, default=128)
     ap.add_argument("--tokens", type=int, default=4096)
@@ -51,6 +52,14 @@ def main():
         ws = dn.accept_workspace(B, T4, V, dev)
         for _ in range(a.warmup + a.launches):
             dn.dn_accept_greedy(logits, draft, workspace=ws)
+    elif a.kernel == "deltas":
+        x = inputs.recurrence_inputs(a.layers, T, H, d, d, seed=1, device=dev)
+        out = torch.empty_like(x["v"])
+        delta = torch.empty(x["v"].shape, dtype=torch.float32, device=dev)
+        acc = torch.full((1,), 15, dtype=torch.int32, device=dev)
+        for _ in range(a.warmup + a.launches):
+            dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], out, delta)
+            dn.dn_commit_deltas(x["k"], x["g"], delta, acc, x["state"])
     elif a.kernel == "context":
         ctx, lens = inputs.context_inputs(a.requests, a.tokens, 500, V, quote=True, seed=5)
         ctx, lens = ctx.to(dev), lens.to(dev)

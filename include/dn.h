@@ -92,7 +92,7 @@ typedef enum { DN_F16 = 0, DN_F32 = 1 } dn_dtype;
  * The recurrent state of a DeltaNet layer grows with the verify width because
  * each verified position keeps its own state copy, so that any accepted prefix
  * can be committed ([P1]: 1.66 GiB at 15 drafts vs 0.88 GiB at 7; [P2]: a
- * speculating request "reserves recurrent-state pages"). The block is at most
+ * speculating request holds its own pages of recurrent state). The block is at most
  * 16 tokens wide ([P4]).
  *
  * For every state set n < N and head h < H, starting from S = state_in[n][h]:
@@ -124,7 +124,7 @@ dn_status dn_verify_block(int N, int H, int T, int dk, int dv,
  * checkpoints ("recompute on commit").
  *
  * A speculating request reserves a state copy per verified position ([P1]: 1.66 GiB
- * at 15 drafts vs 0.88 GiB at 7; [P2]: "reserves recurrent-state pages"). This pair
+ * at 15 drafts vs 0.88 GiB at 7; [P2]: speculation holds state pages per request). This pair
  * keeps none: verify writes, per position, only the write strength of the delta rule
  *
  *   delta_t = beta_t (v_t - g_t S_{t-1} k_t)        (one fp32 per state row)

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY (see the package docstring for who may import it).
 
 The pages describe the mechanism only in words. "HyperQwen: 1,000 tok/s on a Single
 RTX 3090 ..." (Technical Insight): in single-user mode the later positions of the
-verify block (7 to 14) are filled by copying from the request's own context instead
-of running the drafter, because models often quote their input verbatim. "HyperQwen
+verify block (7 to 14) hold tokens copied out of the prompt and the text generated so
+far rather than drafter proposals, since a model that quotes its input repeats it
+token for token. "HyperQwen
 on one RTX 3090: a first-time developer's guide ..." (What actually became faster?):
 when the output starts copying from the input, a lookup proposes further tokens
 straight from that context. Neither page says how the place to copy from is found.

@@ -151,3 +151,38 @@ def test_prefill_25000_tokens_one_layer(cuda):
     assert_close("out", out[:, :, heads], o_ref, TOL["f16"])
     assert_close("ckpt", ckpt[:, :, heads], c_ref, TOL["f16"])
     assert_close("state_out", s_out[:, heads], s_ref, TOL["f16"])
+
+
+def test_prefill_25000_tokens_all_layers(cuda):
+    """All 48 layers of the 25,000-token prompt in one launch (the launch bench.py times).
+    The oracle checks four seeded heads of every layer over the last two chunks and the
+    40-token tail, restarted from the GPU's own checkpoint at token 24,832, and every head
+    of four layers over the first two chunks from the initial state. (The oracle's explicit
+    dv x dk matrix form costs ~4 MFLOP per token and head, so the full 25,000 tokens of all
+    2,304 units are out of reach; the one-layer test above covers two heads end to end.)"""
+    w = WORKLOADS["prefill_p25000_l48_h48_d128_c64_f16"]
+    L, P, H, d = w["L"], w["P"], w["H"], w["dk"]
+    x = inputs.recurrence_inputs(L, P, H, d, d, seed=w["seed"], device=cuda)
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
+    torch.cuda.synchronize()
+    assert ckpt.shape == (L, 390, H, d, d) and dn.dn_prefill_wait_timeouts() == 0
+
+    start = 64 * 388  # 24,832: two full chunks and the 40-token tail remain
+    gen = torch.Generator().manual_seed(w["seed"] + 1)
+    units = [(n, int(h)) for n in range(L) for h in torch.randperm(H, generator=gen)[:4]]
+    u = {k: np.stack([np64(x[k][n, start:, h]) for n, h in units])[:, :, None] for k in KEYS}
+    s0 = np.stack([np64(ckpt[n, 387, h]) for n, h in units])[:, None]
+    o_ref, c_ref, s_ref = oracle.prefill_checkpoint(u["q"], u["k"], u["v"], u["beta"], u["g"], s0,
+                                                    chunk=64, store="f16", io="f16")
+    assert_close("tail out (every layer)", torch.stack([out[n, start:, h] for n, h in units])[:, :, None],
+                 o_ref, TOL["f16"])
+    assert_close("checkpoints 24,896 and 24,960", torch.stack([ckpt[n, 388:, h] for n, h in units])[:, :, None],
+                 c_ref, TOL["f16"])
+    assert_close("state_out", torch.stack([s_out[n, h] for n, h in units])[:, None], s_ref, TOL["f16"])
+
+    layers, head_len = [0, 17, 31, 47], 128
+    u = {k: np64(x[k][layers, :head_len]) for k in KEYS}
+    o_ref, c_ref, _ = oracle.prefill_checkpoint(u["q"], u["k"], u["v"], u["beta"], u["g"],
+                                                np64(x["state"][layers]), chunk=64, store="f16", io="f16")
+    assert_close("first two chunks out (4 layers, all heads)", out[layers, :head_len], o_ref, TOL["f16"])
+    assert_close("first two checkpoints", ckpt[layers, :head_len // 64], c_ref, TOL["f16"])

@@ -413,6 +413,30 @@ def deltas_row(sets, device, stream, steps=200, warmup=5):
             "algorithmic_bytes_per_step": vb + cb + accept_bytes(B, T, w["V"], 2)}
 
 
+def decode_row(device, stream, steps=1000, warmup=10, nsets=8):
+    """The single-user decode loop: 1000 consecutive verify (T = 8) -> accept -> commit steps
+    timed as one loop, each step committing into the state the next step of its buffer set
+    reads. Accepted lengths are geometric with mean 4, clamped at T (one draw per buffer set;
+    8 rotating sets, ~0.7 GB each, so no step finds its inputs in L2)."""
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS["decode_loop_l48_h48_d128_t8_f16"]
+    sets = make_step_sets(w, device, 0, nsets)
+    secs, per, _ = timed_steps(sets, steps, warmup, stream, None)
+    N, B, T = w["L"] * w["B"], w["B"], w["T"]
+    vb = verify_bytes(N, T, w["H"], w["dk"], w["dv"], 2)
+    plans = [int(x["acc_plan"][0]) for x in sets]
+    cb = statistics.mean(commit_bytes(w["L"], x["acc_plan"], w["H"], w["dk"], w["dv"], 2) for x in sets)
+    res = {"workload": "decode_loop_l48_h48_d128_t8_f16", "steps": steps,
+           "ms_per_step": secs / steps * 1e3, "loop_ms": secs * 1e3,
+           "token_layers_per_s": B * T * w["L"] * steps / secs,
+           "accepted_per_set": plans, "accepted_mean": statistics.mean(plans),
+           "verify_ms": per[0], "verify_gbs": vb / (per[0] / 1e3) / 1e9,
+           "accept_ms": per[1], "commit_ms": per[2],
+           "commit_gbs": cb / (per[2] / 1e3) / 1e9 if per[2] > 0 else None}
+    del sets
+    return res
+
+
 def batch_row(device, stream, steps=10, warmup=3):
     from deltanet_recurrent_state_gb300.workloads import WORKLOADS
     w = WORKLOADS["batch64_l48_h48_d128_t4_f16"]
@@ -611,6 +635,7 @@ def main():
     rows = {}
     if not args.no_rows and rank == 0:
         rows["recompute_on_commit_step"] = deltas_row(sets, device, stream)
+        rows["decode_loop"] = decode_row(device, stream)
         rows["batch64_step"] = batch_row(device, stream)
         rows["prefill"] = prefill_row(device, stream)
         rows["context_drafts"] = context_row(device, stream)
@@ -660,9 +685,11 @@ def main():
                      "frac_of_nominal_8tbs": achieved / 8000.0, "traffic": traffic,
                      "algorithmic_bytes_per_launch": vb, "ms_per_launch": v_ms},
         "kernels": {
-            "dn_verify_block": {"ms": v_ms, "gbs": achieved, "bytes": vb},
-            "dn_accept_greedy": {"ms": a_ms, "gbs": ab / (a_ms / 1e3) / 1e9, "bytes": ab},
-            "dn_commit": {"ms": c_ms, "gbs": cb / (c_ms / 1e3) / 1e9, "bytes": cb},
+            "dn_verify_block": {"ms": v_ms, "gbs": achieved, "bytes": vb, "frac": achieved / hbm},
+            "dn_accept_greedy": {"ms": a_ms, "gbs": ab / (a_ms / 1e3) / 1e9, "bytes": ab,
+                                 "frac": ab / (a_ms / 1e3) / 1e9 / hbm},
+            "dn_commit": {"ms": c_ms, "gbs": cb / (c_ms / 1e3) / 1e9, "bytes": cb,
+                          "frac": cb / (c_ms / 1e3) / 1e9 / hbm},
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_k},

@@ -267,39 +267,108 @@ def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True):
     return secs, per, (t_wall0, t_wall1)
 
 
-def e2e_steps(w, sets, steps, warmup, stream, device):
+def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True):
     """The same step through the public API with host inputs: every step copies its
-    inputs from pinned host memory and reads its results back (out, target ids,
-    accepted length) before the next step starts."""
+    inputs from pinned host memory and reads its results back (the target ids and the
+    accepted length, which a serving loop needs to emit tokens; the outputs o feed the
+    next sub-layer on the device), and the host waits for them before the next step. A step's
+    inputs sit in one pinned buffer and its results in one device region (the tensors the
+    calls take are views of them), so each direction is a single copy.
+    With `graphs`, each buffer set's step (its host-to-device copies, the three calls
+    and the device-to-host copies, all issued through the public binding) is captured
+    once in a CUDA graph, and a step is one replay; otherwise every call is issued from
+    Python each step. Returns (seconds, h2d bytes per step, d2h bytes per step)."""
     import torch
     from deltanet_recurrent_state_gb300 import binding as dn
     in_keys = ("q", "k", "v", "beta", "g", "logits", "draft")
-    host = [{k: x[k].cpu().pin_memory() for k in in_keys} for x in sets]
-    outs = [{k: torch.empty(x[k].shape, dtype=x[k].dtype).pin_memory() for k in ("out", "tgt", "acc")}
-            for x in sets]
-    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in in_keys)
-    d2h = sum(outs[0][k].numel() * outs[0][k].element_size() for k in outs[0])
+    out_keys = ("tgt", "acc")  # what the serving loop needs back; o stays on the device
 
-    def one(i):
-        x, h, o = sets[i % len(sets)], host[i % len(sets)], outs[i % len(sets)]
+    def packed(x, keys, pinned):
+        """One byte buffer holding the tensors `keys` of x (256-byte aligned), and views of
+        it with their shapes and dtypes."""
+        offs, total = {}, 0
+        for k in keys:
+            offs[k] = total
+            total += (x[k].numel() * x[k].element_size() + 255) // 256 * 256
+        buf = torch.empty(total, dtype=torch.uint8, pin_memory=pinned) if pinned else \
+            torch.empty(total, dtype=torch.uint8, device=device)
+        views = {k: buf[offs[k]:offs[k] + x[k].numel() * x[k].element_size()].view(x[k].dtype)
+                 .view(x[k].shape) for k in keys}
+        return buf, views
+
+    # per buffer set: device inputs and results as views of one region each, so a step is
+    # one host-to-device and one device-to-host copy
+    host, dev_in, dev_out, host_out = [], [], [], []
+    for x in sets:
+        hb, hv = packed(x, in_keys, True)
+        db, dv_ = packed(x, in_keys, False)
+        for k in in_keys:
+            hv[k].copy_(x[k].cpu())
+            dv_[k].copy_(x[k])
+        ob, ov = packed(x, out_keys, False)
+        hob, hov = packed(x, out_keys, True)
+        host.append(hb)
+        dev_in.append((db, dv_))
+        dev_out.append((ob, ov))
+        host_out.append(hob)
+    h2d = host[0].numel()
+    d2h = host_out[0].numel()
+
+    side = [torch.cuda.Stream(device) for _ in range(4)]
+
+    def body(j):
+        x = dict(sets[j])
+        x.update(dev_in[j][1])
+        x.update(dev_out[j][1])
+        # the inputs in four concurrent pieces (several copy engines), joined before the calls
+        n = host[j].numel()
+        cut = [0] + [(n * i // 4 + 255) // 256 * 256 for i in (1, 2, 3)] + [n]
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        joins = []
+        for i, ss in enumerate(side):
+            ss.wait_event(fork)
+            with torch.cuda.stream(ss):
+                dev_in[j][0][cut[i]:cut[i + 1]].copy_(host[j][cut[i]:cut[i + 1]], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(ss)
+            joins.append(e)
+        for e in joins:
+            stream.wait_event(e)
+        dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                           x["ckpt"], stream=stream)
+        dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+        dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
+        host_out[j].copy_(dev_out[j][0], non_blocking=True)
+
+    def eager(i):
         with torch.cuda.stream(stream):
-            for k in in_keys:
-                x[k].copy_(h[k], non_blocking=True)
-            dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
-                               x["ckpt"], stream=stream)
-            dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"],
-                                stream=stream)
-            dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
-            for k in ("out", "tgt", "acc"):
-                o[k].copy_(x[k], non_blocking=True)
+            body(i % len(sets))
         stream.synchronize()
 
     for i in range(warmup):
-        one(i)
+        eager(i)
     torch.cuda.synchronize()
+    step = eager
+    if graphs:
+        gs = []
+        for j in range(len(sets)):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                body(j)
+            gs.append(gr)
+
+        def step(i):
+            with torch.cuda.stream(stream):
+                gs[i % len(sets)].replay()
+            stream.synchronize()
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        one(i)
+        step(i)
     torch.cuda.synchronize()
     return time.perf_counter() - t0, h2d, d2h
 
@@ -631,6 +700,7 @@ def main():
     e2e_k = max(3, min(args.steps, 200))
     e2e_s, h2d, d2h = e2e_steps(w, sets, e2e_k, 3, stream, device)
     e2e_value = B * T * w["L"] * e2e_k / e2e_s
+    e2e_eager_s, _, _ = e2e_steps(w, sets, e2e_k, 3, stream, device, graphs=False)
 
     rows = {}
     if not args.no_rows and rank == 0:
@@ -692,7 +762,11 @@ def main():
                           "frac": cb / (c_ms / 1e3) / 1e9 / hbm},
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_k},
+                "d2h_bytes_per_step": d2h, "steps": e2e_k,
+                "how": "one CUDA graph replay per step (host-to-device inputs as four concurrent "
+                       "copies, the three calls, device-to-host target ids and accepted length); "
+                       "the host waits for each step's results",
+                "eager_value": B * T * w["L"] * e2e_k / e2e_eager_s},
         "gpu_launches": 3 * args.steps,
         "clocks": clock_info,
         "cpu_baseline": cpu,

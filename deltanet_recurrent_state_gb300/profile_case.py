@@ -3,7 +3,7 @@
     python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3]
     python -m deltanet_recurrent_state_gb300.profile_case accept  [--requests 128]
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
-    python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1]
+    python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1] [--engine mma|tc]
     python -m deltanet_recurrent_state_gb300.profile_case context [--tokens 268000] [--requests 64]
     python -m deltanet_recurrent_state_gb300.profile_case deltas  [--layers 8]
 
@@ -33,6 +33,7 @@ def main():
     ap.add_argument("--sequences", type=int, default=1)
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--engine", choices=["mma", "tc"], default="mma", help="prefill engine")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     H, d, T, V = 48, 128, 16, 151936
@@ -68,7 +69,7 @@ def main():
     else:
         x = inputs.recurrence_inputs(a.sequences, a.tokens, H, d, d, seed=4, device=dev)
         for _ in range(a.warmup + a.launches):
-            dn.dn_prefill_checkpoint(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+            dn.dn_prefill_checkpoint(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], engine=a.engine)
     torch.cuda.synchronize()
     print("profile_case %s done" % a.kernel)
 

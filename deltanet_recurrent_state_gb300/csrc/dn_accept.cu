@@ -15,6 +15,7 @@
 // them, so the workspace is ready for the next call. Nothing spins or waits.
 #include <mutex>
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "dn.h"
@@ -122,14 +123,43 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
             const int i = threadIdx.x + r * kThreads;
             if (i < nvec) u[r] = __ldcs(vp + i);
         }
+        if constexpr (VEC == 8) {
+            // fp16: the thread's maximum by packed max, then the lowest index holding it (its
+            // elements are in increasing index order); -0 and +0 compare equal, as numbers do
+            const __half2 lowest = __halves2half2(__ushort_as_half(0xfbffu), __ushort_as_half(0xfbffu));
+            __half2 m2 = lowest;
 #pragma unroll
-        for (int r = 0; r < kPer; ++r) {
-            const int i = threadIdx.x + r * kThreads;
-            if (i < nvec) {
-                const E *e = reinterpret_cast<const E *>(&u[r]);
-                const int base = c0 + i * VEC;
+            for (int r = 0; r < kPer; ++r) {
+                const int i = threadIdx.x + r * kThreads;
+                if (i < nvec) {
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&u[r]);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) best = umax64(best, pack_key(order_key(e[j]), base + j));
+                    for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, h2[j]);
+                }
+            }
+            const __half m = __hmax(__low2half(m2), __high2half(m2));
+            int idx = -1;
+#pragma unroll
+            for (int r = kPer - 1; r >= 0; --r) {
+                const int i = threadIdx.x + r * kThreads;
+                if (i < nvec) {
+                    const __half *e = reinterpret_cast<const __half *>(&u[r]);
+#pragma unroll
+                    for (int j = VEC - 1; j >= 0; --j)
+                        if (__heq(e[j], m)) idx = c0 + i * VEC + j;
+                }
+            }
+            if (idx >= 0) best = pack_key(order_key(__half_as_ushort(m)), idx);
+        } else {
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) {
+                const int i = threadIdx.x + r * kThreads;
+                if (i < nvec) {
+                    const E *e = reinterpret_cast<const E *>(&u[r]);
+                    const int base = c0 + i * VEC;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) best = umax64(best, pack_key(order_key(e[j]), base + j));
+                }
             }
         }
         done = c0 + nvec * VEC;

@@ -466,17 +466,33 @@ def deltas_row(sets, device, stream, steps=200, warmup=5):
     with torch.cuda.stream(stream):
         for i in range(warmup):
             step(sets[i % len(sets)])
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    # the timed steps are CUDA graph replays (one per buffer set), as for the main step
+    gs = []
+    for x in sets:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(x)
+        gs.append(gr)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            gs[i % len(gs)].replay()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     s0.record(stream)
     with torch.cuda.stream(stream):
         for i in range(steps):
-            step(sets[i % len(sets)], evs[i])
+            gs[i % len(gs)].replay()
     s1.record(stream)
     torch.cuda.synchronize()
     secs = s0.elapsed_time(s1) / 1e3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(sets[i % len(sets)], evs[i])
+    torch.cuda.synchronize()
     per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(3)]
+    del gs
     vb = verify_deltas_bytes(N, T, H, dk, dv, 2)
     cb = commit_deltas_bytes(w["L"], sets[0]["acc_plan"], H, dk, dv, 2)
     for x in sets:

@@ -154,8 +154,10 @@ __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
 
 // CKPT: write the T checkpoints (dn_verify_block); otherwise write delta_t instead
 // (dn_verify_block_deltas), from which dn_commit_deltas rebuilds the accepted state.
-template <int DK, bool CKPT>
-__global__ void __launch_bounds__(256, 5)
+// TM: the block capacity the shared tiles are sized for (16, or 8 for blocks of up to 8
+// tokens, whose smaller tiles let more CTAs share an SM).
+template <int DK, bool CKPT, int TM>
+__global__ void __launch_bounds__(256, TM == 8 ? 6 : 5)
 verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
                  const __half *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ g, const __half *__restrict__ s_in,
@@ -165,13 +167,13 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     constexpr int NCH = CPR / TPR;     // chunks per lane
     constexpr int KS = DK / 16;        // MMA k-steps
     __shared__ __align__(128) uint4 sS0[ROWS * CPR];
-    __shared__ __align__(128) uint4 sKQ[2 * kMaxT * CPR];  // rows 0..15 k_t, 16..31 q_t
-    __shared__ __align__(16) float sk[kMaxT][DK];           // k_t in fp32 (swz4)
-    __shared__ float proj[ROWS][2 * kMaxT + 1];              // [row][t] S0 k_t, [row][16+t] S0 q_t
-    __shared__ float gram[2 * kMaxT][kMaxT + 1];             // [t][s] k_t.k_s, [16+t][s] q_t.k_s
-    __shared__ float sL[kMaxT][kMaxT], sM[kMaxT][kMaxT];
-    __shared__ float sgam[kMaxT], sG[kMaxT], sbeta[kMaxT], sg[kMaxT];
-    __shared__ float sv[kMaxT][ROWS], sd[kMaxT][ROWS], so[kMaxT][ROWS];
+    __shared__ __align__(128) uint4 sKQ[2 * TM * CPR];  // rows 0..TM-1 k_t, TM..2TM-1 q_t
+    __shared__ __align__(16) float sk[TM][DK];           // k_t in fp32 (swz4)
+    __shared__ float proj[ROWS][2 * TM + 1];              // [row][t] S0 k_t, [row][TM+t] S0 q_t
+    __shared__ float gram[2 * TM][TM + 1];                // [t][s] k_t.k_s, [TM+t][s] q_t.k_s
+    __shared__ float sL[TM][TM], sM[TM][TM];
+    __shared__ float sgam[TM], sG[TM], sbeta[TM], sg[TM];
+    __shared__ float sv[TM][ROWS], sd[TM][ROWS], so[TM][ROWS];
 
     const int rblocks = DV / ROWS;
     const int rb = blockIdx.x % rblocks;
@@ -195,7 +197,7 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
         }
     }
-    for (int i = tid; i < kMaxT * CPR; i += NT) {
+    for (int i = tid; i < TM * CPR; i += NT) {
         const int t = i / CPR, j = i % CPR;
         uint4 uk = make_uint4(0u, 0u, 0u, 0u), uq = uk;  // rows past T stay zero
         if (t < T) {
@@ -213,7 +215,7 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             smem_put8(sk[t], j, x);
         }
         sKQ[hsw<CPR>(t, j)] = uk;
-        sKQ[hsw<CPR>(kMaxT + t, j)] = uq;
+        sKQ[hsw<CPR>(TM + t, j)] = uq;
     }
     for (int i = tid; i < T * ROWS; i += NT) {
         const int t = i / ROWS, r = i % ROWS;
@@ -228,11 +230,11 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             lg = logf(fmaxf(gg, 1e-30f));
         }
 #pragma unroll
-        for (int off = 1; off < kMaxT; off <<= 1) {
+        for (int off = 1; off < TM; off <<= 1) {
             const float o = __shfl_up_sync(0xffffffffu, lg, off);
             if (lane >= off) lg += o;
         }
-        if (lane < kMaxT) {
+        if (lane < TM) {
             sG[lane] = lg;
             sgam[lane] = expf(lg);
             sg[lane] = gg;
@@ -241,8 +243,9 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     }
     __syncthreads();
 
-    // 2. proj = S0 [K;Q]^T (8 warps, one 16x8 tile each); gram = [K;Q] K^T (warps 0..3)
-    {
+    // 2. proj = S0 [K;Q]^T (one 16x8 tile per warp); gram = [K;Q] K^T (one tile per warp)
+    constexpr int NG = TM / 8, MG = 2 * TM / 16;  // gram tiles: n (tokens of K), m (rows of [K;Q])
+    if ((warp & 3) * 8 < 2 * TM) {
         const int mt = warp >> 2, nt = warp & 3;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -257,8 +260,8 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         proj[r0][c0 + 1] = d[1];
         proj[r0 + 8][c0] = d[2];
         proj[r0 + 8][c0 + 1] = d[3];
-        if (warp < 4) {
-            const int gm = warp >> 1, gn = warp & 1;
+        if (warp < MG * NG) {
+            const int gm = warp / NG, gn = warp % NG;
             float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -277,19 +280,19 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     __syncthreads();
 
     // 3. L (strictly lower) and M (lower incl. diagonal), one entry per thread
-    {
-        const int t = tid >> 4, s2 = tid & 15;
+    if (tid < TM * TM) {
+        const int t = tid / TM, s2 = tid % TM;
         const float r = (s2 <= t) ? expf(sG[t] - sG[s2]) : 0.f;
         sL[t][s2] = (s2 < t) ? r * gram[t][s2] : 0.f;
-        sM[t][s2] = r * gram[kMaxT + t][s2];
+        sM[t][s2] = r * gram[TM + t][s2];
     }
     __syncthreads();
 
     // 4. delta_t by forward substitution, one lane per row
     if (warp == 0) {
-        float dl[kMaxT];
+        float dl[TM];
 #pragma unroll
-        for (int t = 0; t < kMaxT; ++t) {
+        for (int t = 0; t < TM; ++t) {
             dl[t] = 0.f;
             if (t < T) {
                 float acc = 0.f;
@@ -331,7 +334,7 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     // 6. outputs
     for (int i = tid; i < T * ROWS; i += NT) {
         const int t = i / ROWS, r = i % ROWS;
-        float o = sgam[t] * proj[r][kMaxT + t];
+        float o = sgam[t] * proj[r][TM + t];
         for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
         so[t][r] = o;
     }
@@ -381,10 +384,14 @@ extern "C" dn_status dn_verify_block(int N, int H, int T, int dk, int dv, dn_dty
         const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
         const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
         __half *oh = static_cast<__half *>(out), *ch = static_cast<__half *>(ckpt);
-        if (dk == 128)
-            verify_wy_kernel<128, true><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+        if (dk == 128 && T <= 8)
+            verify_wy_kernel<128, true, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+        else if (dk == 128)
+            verify_wy_kernel<128, true, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+        else if (T <= 8)
+            verify_wy_kernel<64, true, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
         else
-            verify_wy_kernel<64, true><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+            verify_wy_kernel<64, true, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
     } else {
         if (dk == 128) launch_verify<128, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
         else launch_verify<64, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
@@ -413,9 +420,13 @@ extern "C" dn_status dn_verify_block_deltas(int N, int H, int T, int dk, int dv,
     const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
     const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
     __half *oh = static_cast<__half *>(out);
-    if (dk == 128)
-        verify_wy_kernel<128, false><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+    if (dk == 128 && T <= 8)
+        verify_wy_kernel<128, false, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+    else if (dk == 128)
+        verify_wy_kernel<128, false, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+    else if (T <= 8)
+        verify_wy_kernel<64, false, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
     else
-        verify_wy_kernel<64, false><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+        verify_wy_kernel<64, false, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
     return launch_status();
 }

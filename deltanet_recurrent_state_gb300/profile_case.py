@@ -1,6 +1,6 @@
 """Run one libdn kernel on a small case for profiling (a few launches, inputs > L2).
 
-    python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3]
+    python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3] [--T 16]
     python -m deltanet_recurrent_state_gb300.profile_case accept  [--requests 128]
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
     python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1] [--engine mma|tc]
@@ -34,13 +34,14 @@ def main():
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--engine", choices=["mma", "tc"], default="mma", help="prefill engine")
+    ap.add_argument("--T", type=int, default=16, help="verify block width")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
-    H, d, T, V = 48, 128, 16, 151936
+    H, d, T, V = 48, 128, a.T, 151936
     if a.kernel in ("verify", "commit"):
         x = inputs.recurrence_inputs(a.layers, T, H, d, d, seed=1, device=dev)
         out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
-        acc = torch.full((1,), 15, dtype=torch.int32, device=dev)
+        acc = torch.full((1,), T - 1, dtype=torch.int32, device=dev)
         for _ in range(a.warmup + a.launches):
             if a.kernel == "verify":
                 dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], out, ckpt)

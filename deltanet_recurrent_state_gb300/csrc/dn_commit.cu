@@ -52,9 +52,10 @@ commit_kernel(int B, int T, size_t set_bytes, const uint4 *__restrict__ ckpt,
 // S_a = g_{a-1} ( ... (g_0 S_0 + delta_0 k_0^T) ... ) + delta_{a-1} k_{a-1}^T, applied here
 // to the old state in place with exactly the arithmetic (packed fp32x2 FMAs in the same
 // order) the checkpoint path uses, so both paths commit bit-identical states. A CTA owns
-// 32 rows of one (state set, head), 8 lanes per row, 16 fp32 elements per lane.
+// 32 rows of one (state set, head), 8 lanes per row, 16 fp32 elements per lane; six CTAs
+// share an SM so that one's loads overlap the others' replays.
 template <int DK>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 6)
 commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
                      const float *__restrict__ g, const float *__restrict__ delta,
                      const int *__restrict__ accepted, __half *__restrict__ state) {

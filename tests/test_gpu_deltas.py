@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
-@pytest.mark.parametrize("T", [1, 7, 16])
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 16])
 def test_deltas_path_equals_checkpoint_path(dk, dv, T, cuda):
     L, B, H = 2, T + 1, 3          # request b accepts b tokens: every length 0..T
     N = L * B

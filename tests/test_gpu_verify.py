@@ -33,7 +33,7 @@ def test_tiny_fp32_workload(cuda):
     _run_case(1, 8, 4, 64, 64, "f32", 1000, cuda)
 
 
-@pytest.mark.parametrize("T", [1, 2, 5, 8, 15, 16])
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 9, 15, 16])
 def test_fp16_d128_every_width(T, cuda):
     _run_case(3, T, 5, 128, 128, "f16", 10 + T, cuda)
 

@@ -204,8 +204,27 @@ __device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
 // inputs and products are ready, EMPTY[p] (chain arrives, prep waits) when the
 // chain is done with them. Inputs are triple buffered (chunk c, chunk c+1 and the
 // load of the next one), the prep products double buffered.
-constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6;
-constexpr int kPrepThreads = 128;
+// Issuing a TMA copy holds its thread for a hundred or more cycles (a chunk's six input
+// boxes about 1,300 cycles, its four output and checkpoint boxes about 450), and issuing
+// them from several warps at once is no faster. Where registers allow, a producer warp
+// issues every copy, off both roles' critical paths: it loads chunk c+3 once the chain is
+// done with chunk c (EMPTY), stores chunk c's output and checkpoint boxes once the chain
+// has staged them (STORE), and when those stores have read shared memory tells the chain
+// (STORE_FREE), which waits for that before staging the next checkpoint. Otherwise prep
+// thread 0 issues the loads and chain thread 0 the stores.
+constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6, kBarStore = 7, kBarStoreFree = 8;
+constexpr int kPrepThreads = 128, kProducerThreads = 32;
+
+// A thirteenth warp caps every thread of the CTA at 128 registers (the register file is
+// split between the SM's four schedulers and one of them then holds four warps); the
+// chain warps of a dk = 128 state over 128 rows want about 157 and measure slower
+// squeezed, so that instance goes without the producer warp.
+template <int DK, int DVC>
+constexpr bool prefill_producer() { return !(DK == 128 && DVC == 128); }
+template <int DK, int DVC, int RT>
+constexpr int prefill_threads() {
+    return DVC * 2 / RT + kPrepThreads + (prefill_producer<DK, DVC>() ? kProducerThreads : 0);
+}
 constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
 // 16-row state tiles per chain warp. Two tiles per warp halve the operand fragments each
 // warp loads from shared memory but measure no faster on GB300 (the chain is bound by the
@@ -220,13 +239,15 @@ struct PrefillMaps {
 };
 
 template <int DK, int DV, int DVC, int RT>
-__global__ void __launch_bounds__(DVC * 2 / RT + kPrepThreads, 1)
+__global__ void __launch_bounds__(prefill_threads<DK, DVC, RT>(), 1)
 prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                   const float *__restrict__ beta, const float *__restrict__ g,
                   const __half *s_in, __half *s_out) {
     using L = PrefillSmem<DK, DVC>;
     constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
     constexpr int NW = DVC / (16 * RT), NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
+    constexpr bool PROD = prefill_producer<DK, DVC>();
+    constexpr int NTX = PROD ? kProducerThreads : 0;  // the producer warp follows the prep warps
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
     constexpr int BOXU = C * 8;   // uint4 per 64 x 64 box
@@ -262,21 +283,60 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
     __syncthreads();
 
+    // chunk c's q/k/v boxes on mbar[c % 3] (rows past the prompt arrive as zeros)
+    auto load_chunk = [&](int c) {
+        const int p0 = c * C, kb = c % 3;
+        mbar_arrive_expect_tx(&mbar[kb], (unsigned)((2 * KH + VH) * L::kBox));
+        for (int x = 0; x < KH; ++x) {
+            tma_load_4d(sK + (kb * KH + x) * BOXU, &maps.k, 64 * x, h, p0, n, &mbar[kb]);
+            tma_load_4d(sQ + (kb * KH + x) * BOXU, &maps.q, 64 * x, h, p0, n, &mbar[kb]);
+        }
+        for (int x = 0; x < VH; ++x)
+            tma_load_4d(sV + (kb * VH + x) * BOXU, &maps.v, r0 + 64 * x, h, p0, n, &mbar[kb]);
+    };
+    // chunk c's output boxes O[c & 1], and its checkpoint box when the chunk is full
+    auto store_chunk = [&](int c) {
+        const int p0 = c * C;
+        const uint4 *cO = sO + (c & 1) * VH * BOXU;
+        for (int x = 0; x < VH; ++x) tma_store_4d(&maps.o, r0 + 64 * x, h, p0, n, cO + x * BOXU);
+        if (P - p0 >= C)
+            for (int x = 0; x < KH; ++x)
+                tma_store_3d(&maps.ck, 64 * x, r0, (n * nfull + c) * H + h, sCk + x * DVC * 8);
+        bulk_commit();
+    };
+
+    if constexpr (PROD) {
+        if (warp == NW + NTP / 32) {
+            // ============================= producer warp =============================
+            if (lane == 0)
+                for (int c = 0; c < min(3, nchunks); ++c) load_chunk(c);
+            for (int c = 0; c < nchunks; ++c) {
+                if (c + 2 < nchunks) {
+                    bar_sync(kBarEmpty + (c & 1), NTALL + NTX);  // inputs[c % 3] consumed
+                    if (c + 3 < nchunks && lane == 0) load_chunk(c + 3);
+                }
+                bar_sync(kBarStore, NTC + NTX);  // chunk c's output (and checkpoint) boxes staged
+                if (lane == 0) store_chunk(c);
+                if (c + 1 < nchunks) {
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                    bar_arrive(kBarStoreFree, NTC + NTX);  // the checkpoint box and O[c & 1] free again
+                }
+            }
+            if (lane == 0) bulk_wait();
+            return;
+        }
+    }
+
     if (warp >= NW) {
         // ============================== prep warps ==============================
         const int pt = tid - NTC, pw = pt / 32;
-        // chunk c: q/k/v boxes by the TMA engine on mbar[c % 3] (rows past the prompt
-        // arrive as zeros), beta and g by 4-byte cp.async (zeros past the prompt)
+        // chunk c: q/k/v by the TMA engine (from the producer warp when there is one),
+        // beta and g by 4-byte cp.async (zeros past the prompt)
         auto issue = [&](int c) {
             const int p0 = c * C, kb = c % 3;
-            if (pt == 0) {
-                mbar_arrive_expect_tx(&mbar[kb], (unsigned)((2 * KH + VH) * L::kBox));
-                for (int x = 0; x < KH; ++x) {
-                    tma_load_4d(sK + (kb * KH + x) * BOXU, &maps.k, 64 * x, h, p0, n, &mbar[kb]);
-                    tma_load_4d(sQ + (kb * KH + x) * BOXU, &maps.q, 64 * x, h, p0, n, &mbar[kb]);
-                }
-                for (int x = 0; x < VH; ++x)
-                    tma_load_4d(sV + (kb * VH + x) * BOXU, &maps.v, r0 + 64 * x, h, p0, n, &mbar[kb]);
+            if constexpr (!PROD) {
+                if (pt == 0) load_chunk(c);
             }
             const size_t row0 = ((size_t)n * P + p0) * H + h;
             for (int i = pt; i < 2 * C; i += NTP) {
@@ -291,7 +351,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         cp_async_commit();
         for (int c = 0; c < nchunks; ++c) {
             const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3;
-            if (c >= 2) bar_sync(kBarEmpty + pb, NTALL);  // chunk c-2 done: products[pb], inputs[(c+1)%3] free
+            if (c >= 2) bar_sync(kBarEmpty + pb, NTALL + NTX);  // chunk c-2 done: products[pb], gates[(c+1)%3] free
             if (c + 1 < nchunks) issue(c + 1);
             cp_async_commit();
             cp_async_wait<1>();
@@ -514,10 +574,14 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 }
             }
         }
-        if (c + 2 < nchunks) bar_arrive(kBarEmpty + pb, NTALL);  // inputs / products of chunk c consumed
-        // The previous chunk's TMA stores have read the checkpoint box (and O boxes).
-        if (tid == 0) bulk_wait_read();
-        bar_sync(kBarChain, NTC);
+        if (c + 2 < nchunks) bar_arrive(kBarEmpty + pb, NTALL + NTX);  // inputs / products of chunk c consumed
+        // The previous chunk's TMA stores have read the checkpoint box (and O[ob ^ 1]).
+        if constexpr (PROD) {
+            if (c >= 1) bar_sync(kBarStoreFree, NTC + NTX);
+        } else {
+            if (tid == 0) bulk_wait_read();
+            bar_sync(kBarChain, NTC);
+        }
         if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged for the TMA store
 #pragma unroll
             for (int mt = 0; mt < RT; ++mt)
@@ -540,16 +604,16 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 }
         }
         fence_proxy_async();
-        bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
-        if (tid == 0) {
-            for (int x = 0; x < VH; ++x) tma_store_4d(&maps.o, r0 + 64 * x, h, p0, n, cO + x * BOXU);
-            if (nc == C)
-                for (int x = 0; x < KH; ++x)
-                    tma_store_3d(&maps.ck, 64 * x, r0, (n * nfull + c) * H + h, sCk + x * DVC * 8);
-            bulk_commit();
+        if constexpr (PROD) {
+            bar_arrive(kBarStore, NTC + NTX);  // O boxes and checkpoint boxes staged for the producer
+        } else {
+            bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
+            if (tid == 0) store_chunk(c);
         }
     }
-    if (tid == 0) bulk_wait();
+    if constexpr (!PROD) {
+        if (tid == 0) bulk_wait();
+    }
 #pragma unroll
     for (int mt = 0; mt < RT; ++mt)
 #pragma unroll
@@ -607,7 +671,8 @@ dn_status launch_prefill_wy_split(int N, int H, int P, const void *q, const void
         const cuuint32_t box3[3] = {64, (cuuint32_t)DVC, 1};
         if (!encode_map(&maps.ck, ckpt, 3, dims, str, box3)) return DN_ERR_CUDA;
     }
-    prefill_wy_kernel<DK, DV, DVC, RT><<<(unsigned)((long long)N * H * (DV / DVC)), DVC * 2 / RT + kPrepThreads, bytes,
+    prefill_wy_kernel<DK, DV, DVC, RT><<<(unsigned)((long long)N * H * (DV / DVC)),
+                                      prefill_threads<DK, DVC, RT>(), bytes,
                                       st>>>(
         H, P, maps, beta, g, static_cast<const __half *>(s_in), static_cast<__half *>(s_out));
     return DN_OK;

@@ -206,25 +206,36 @@ __device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
 // load of the next one), the prep products double buffered.
 // Issuing a TMA copy holds its thread for a hundred or more cycles (a chunk's six input
 // boxes about 1,300 cycles, its four output and checkpoint boxes about 450), and issuing
-// them from several warps at once is no faster. Where registers allow, a producer warp
-// issues every copy, off both roles' critical paths: it loads chunk c+3 once the chain is
-// done with chunk c (EMPTY), stores chunk c's output and checkpoint boxes once the chain
-// has staged them (STORE), and when those stores have read shared memory tells the chain
-// (STORE_FREE), which waits for that before staging the next checkpoint. Otherwise prep
-// thread 0 issues the loads and chain thread 0 the stores.
-constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarChain = 6, kBarStore = 7, kBarStoreFree = 8;
+// them from several warps at once is no faster. A producer warp issues every copy, off
+// both roles' critical paths: it loads chunk c+3 once the chain is done with chunk c
+// (EMPTY), stores chunk c's output and checkpoint boxes once the chain has staged them
+// (STORE), and when those stores have read shared memory tells the chain (STORE_FREE),
+// which waits for that before staging the next checkpoint.
+constexpr int kBarFull = 1, kBarEmpty = 3, kBarPrep = 5, kBarStore = 6, kBarStoreFree = 7;
 constexpr int kPrepThreads = 128, kProducerThreads = 32;
 
-// A thirteenth warp caps every thread of the CTA at 128 registers (the register file is
-// split between the SM's four schedulers and one of them then holds four warps); the
-// chain warps of a dk = 128 state over 128 rows want about 157 and measure slower
-// squeezed, so that instance goes without the producer warp.
+// A thirteenth warp caps every thread of the CTA at 128 registers: the register file is
+// split between the SM's four schedulers, and one of them then holds four warps. The chain
+// warps of a dk = 128 state over 128 rows want about 157 and measure slower squeezed, so
+// that CTA is launched as four whole warpgroups (512 threads at 128 registers each) and
+// the registers are redistributed by warpgroup: the producer's warpgroup drops to
+// kProducerRegs and three of its warps leave, the two chain warpgroups rise to
+// kChainRegs, the prep warpgroup keeps 128. Per scheduler that is 2 x 168 + 128 + 24 =
+// 488 of its 512 registers per thread slot (62,464 of the CTA's 65,536), so the rise
+// never waits on registers that are not there.
+constexpr int kChainRegs = 168, kProducerRegs = 24;
 template <int DK, int DVC>
-constexpr bool prefill_producer() { return !(DK == 128 && DVC == 128); }
+constexpr bool prefill_regsplit() { return DK == 128 && DVC == 128; }
 template <int DK, int DVC, int RT>
 constexpr int prefill_threads() {
-    return DVC * 2 / RT + kPrepThreads + (prefill_producer<DK, DVC>() ? kProducerThreads : 0);
+    return DVC * 2 / RT + kPrepThreads + (prefill_regsplit<DK, DVC>() ? 4 * kProducerThreads : kProducerThreads);
 }
+static_assert(2 * kChainRegs + 65536 / 512 + kProducerRegs <= 512, "register split exceeds a scheduler's file");
+
+template <int N>
+__device__ __forceinline__ void regs_raise() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_lower() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
 // 16-row state tiles per chain warp. Two tiles per warp halve the operand fragments each
 // warp loads from shared memory but measure no faster on GB300 (the chain is bound by the
@@ -246,8 +257,9 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     using L = PrefillSmem<DK, DVC>;
     constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
     constexpr int NW = DVC / (16 * RT), NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
-    constexpr bool PROD = prefill_producer<DK, DVC>();
-    constexpr int NTX = PROD ? kProducerThreads : 0;  // the producer warp follows the prep warps
+    constexpr bool SPLIT = prefill_regsplit<DK, DVC>();
+    static_assert(!SPLIT || (NW == 8 && kPrepThreads == 128), "the register split assumes 2 + 1 + 1 warpgroups");
+    constexpr int NTX = kProducerThreads;  // the producer warp follows the prep warps
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection
     constexpr int BOXU = C * 8;   // uint4 per 64 x 64 box
@@ -305,39 +317,38 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         bulk_commit();
     };
 
-    if constexpr (PROD) {
-        if (warp == NW + NTP / 32) {
-            // ============================= producer warp =============================
-            if (lane == 0)
-                for (int c = 0; c < min(3, nchunks); ++c) load_chunk(c);
-            for (int c = 0; c < nchunks; ++c) {
-                if (c + 2 < nchunks) {
-                    bar_sync(kBarEmpty + (c & 1), NTALL + NTX);  // inputs[c % 3] consumed
-                    if (c + 3 < nchunks && lane == 0) load_chunk(c + 3);
-                }
-                bar_sync(kBarStore, NTC + NTX);  // chunk c's output (and checkpoint) boxes staged
-                if (lane == 0) store_chunk(c);
-                if (c + 1 < nchunks) {
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
-                    bar_arrive(kBarStoreFree, NTC + NTX);  // the checkpoint box and O[c & 1] free again
-                }
-            }
-            if (lane == 0) bulk_wait();
-            return;
+    if (warp >= NW + NTP / 32) {
+        // ============================= producer warp =============================
+        if constexpr (SPLIT) {
+            regs_lower<kProducerRegs>();  // the whole warpgroup, then its spare warps leave
+            if (warp != NW + NTP / 32) return;
         }
+        if (lane == 0)
+            for (int c = 0; c < min(3, nchunks); ++c) load_chunk(c);
+        for (int c = 0; c < nchunks; ++c) {
+            if (c + 2 < nchunks) {
+                bar_sync(kBarEmpty + (c & 1), NTALL + NTX);  // inputs[c % 3] consumed
+                if (c + 3 < nchunks && lane == 0) load_chunk(c + 3);
+            }
+            bar_sync(kBarStore, NTC + NTX);  // chunk c's output (and checkpoint) boxes staged
+            if (lane == 0) store_chunk(c);
+            if (c + 1 < nchunks) {
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                bar_arrive(kBarStoreFree, NTC + NTX);  // the checkpoint box and O[c & 1] free again
+            }
+        }
+        if (lane == 0) bulk_wait();
+        return;
     }
 
     if (warp >= NW) {
         // ============================== prep warps ==============================
         const int pt = tid - NTC, pw = pt / 32;
-        // chunk c: q/k/v by the TMA engine (from the producer warp when there is one),
-        // beta and g by 4-byte cp.async (zeros past the prompt)
+        // chunk c: beta and g by 4-byte cp.async (zeros past the prompt); the producer
+        // warp loads q, k and v
         auto issue = [&](int c) {
             const int p0 = c * C, kb = c % 3;
-            if constexpr (!PROD) {
-                if (pt == 0) load_chunk(c);
-            }
             const size_t row0 = ((size_t)n * P + p0) * H + h;
             for (int i = pt; i < 2 * C; i += NTP) {
                 const int which = i / C, t = i % C;
@@ -437,6 +448,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     }
 
     // ============================== chain warps ==============================
+    if constexpr (SPLIT) regs_raise<kChainRegs>();
     // A chain warp owns RT 16-row tiles of the state (rows i0 .. i0 + 16 RT - 1); every
     // operand fragment it loads from shared memory for the projections and the state
     // update serves all RT tiles.
@@ -576,12 +588,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         }
         if (c + 2 < nchunks) bar_arrive(kBarEmpty + pb, NTALL + NTX);  // inputs / products of chunk c consumed
         // The previous chunk's TMA stores have read the checkpoint box (and O[ob ^ 1]).
-        if constexpr (PROD) {
-            if (c >= 1) bar_sync(kBarStoreFree, NTC + NTX);
-        } else {
-            if (tid == 0) bulk_wait_read();
-            bar_sync(kBarChain, NTC);
-        }
+        if (c >= 1) bar_sync(kBarStoreFree, NTC + NTX);
         if (nc == C) {   // chunk end: the carry becomes the fp16 checkpoint, staged for the TMA store
 #pragma unroll
             for (int mt = 0; mt < RT; ++mt)
@@ -604,15 +611,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 }
         }
         fence_proxy_async();
-        if constexpr (PROD) {
-            bar_arrive(kBarStore, NTC + NTX);  // O boxes and checkpoint boxes staged for the producer
-        } else {
-            bar_sync(kBarChain, NTC);  // O boxes and checkpoint boxes complete
-            if (tid == 0) store_chunk(c);
-        }
-    }
-    if constexpr (!PROD) {
-        if (tid == 0) bulk_wait();
+        bar_arrive(kBarStore, NTC + NTX);  // O boxes and checkpoint boxes staged for the producer
     }
 #pragma unroll
     for (int mt = 0; mt < RT; ++mt)

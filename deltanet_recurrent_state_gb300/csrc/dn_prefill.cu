@@ -374,21 +374,33 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
             (void)p0;
             // grams by MMA, tile = (sub-chunk j, K or Q rows) x K_j^T, with the gate scan of
             // the sub-chunk in the same warp; the epilogue applies the decays in registers:
-            // A = beta_t e^{G_t-G_s} k_t.k_s (s < t), Mq = e^{G_t-G_s} q_t.k_s (s <= t)
-            for (int tile = pw; tile < 2 * NSUB; tile += NTP / 32) {
-                const int j = tile >> 1, isq = tile & 1;
-                const uint4 *rows = isq ? cQ : cK;
-                float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+            // A = beta_t e^{G_t-G_s} k_t.k_s (s < t), Mq = e^{G_t-G_s} q_t.k_s (s <= t).
+            // A warp's tiles run their k-loops side by side (independent accumulators).
+            constexpr int TPW = 2 * NSUB / (NTP / 32);  // gram tiles per prep warp
+            float e[TPW][2][4];
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
+            for (int u = 0; u < TPW; ++u)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) e[u][0][w] = e[u][1][w] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int u = 0; u < TPW; ++u) {
+                    const int tile = pw + u * (NTP / 32), j = tile >> 1;
+                    const uint4 *rows = (tile & 1) ? cQ : cK;
                     unsigned a[4], bb[4];
                     ldsm_x4(a, rows + box_chunk(C, 16 * j + (lane & 15), 2 * ks + (lane >> 4)));
                     ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
                                                2 * ks + ((lane >> 3) & 1)));
                     const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
-                    mma_16816(e0, a, b0);
-                    mma_16816(e1, a, b1);
+                    mma_16816(e[u][0], a, b0);
+                    mma_16816(e[u][1], a, b1);
                 }
+#pragma unroll
+            for (int u = 0; u < TPW; ++u) {
+                const int tile = pw + u * (NTP / 32);
+                const int j = tile >> 1, isq = tile & 1;
+                const float *e0 = e[u][0], *e1 = e[u][1];
                 const int tl = 16 * j + (lane & 15);
                 float G = (tl < nc) ? __logf(fmaxf(sgr[tl], 1e-30f)) : 0.f;  // log g, 0 past the prompt
 #pragma unroll
@@ -410,16 +422,16 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 if (!isq) {
                     const float b0r = sbeta[16 * j + fr], b1r = sbeta[16 * j + fr + 8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        sA[j][fr][cs[u]] = (cs[u] < fr) ? b0r * __expf(Gr0 - Gc[u]) * v0[u] : 0.f;
-                        sA[j][fr + 8][cs[u]] = (cs[u] < fr + 8) ? b1r * __expf(Gr1 - Gc[u]) * v1[u] : 0.f;
+                    for (int w = 0; w < 4; ++w) {
+                        sA[j][fr][cs[w]] = (cs[w] < fr) ? b0r * __expf(Gr0 - Gc[w]) * v0[w] : 0.f;
+                        sA[j][fr + 8][cs[w]] = (cs[w] < fr + 8) ? b1r * __expf(Gr1 - Gc[w]) * v1[w] : 0.f;
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        sMq[pb][j][fr][cs[u]] = __float2half_rn((cs[u] <= fr) ? __expf(Gr0 - Gc[u]) * v0[u] : 0.f);
-                        sMq[pb][j][fr + 8][cs[u]] =
-                            __float2half_rn((cs[u] <= fr + 8) ? __expf(Gr1 - Gc[u]) * v1[u] : 0.f);
+                    for (int w = 0; w < 4; ++w) {
+                        sMq[pb][j][fr][cs[w]] = __float2half_rn((cs[w] <= fr) ? __expf(Gr0 - Gc[w]) * v0[w] : 0.f);
+                        sMq[pb][j][fr + 8][cs[w]] =
+                            __float2half_rn((cs[w] <= fr + 8) ? __expf(Gr1 - Gc[w]) * v1[w] : 0.f);
                     }
                 }
             }

@@ -51,16 +51,23 @@ commit_kernel(int B, int T, size_t set_bytes, const uint4 *__restrict__ ckpt,
 // delta_t = beta_t (v_t - g_t S_{t-1} k_t) for every position, and the accepted state is
 // S_a = g_{a-1} ( ... (g_0 S_0 + delta_0 k_0^T) ... ) + delta_{a-1} k_{a-1}^T, applied here
 // to the old state in place with exactly the arithmetic (packed fp32x2 FMAs in the same
-// order) the checkpoint path uses, so both paths commit bit-identical states. A CTA owns
-// 32 rows of one (state set, head), 8 lanes per row, 16 fp32 elements per lane; six CTAs
-// share an SM so that one's loads overlap the others' replays.
+// order) the checkpoint path uses, so both paths commit bit-identical states.
+// A CTA owns 32 rows of one (state set, head): warp w the rows 4w .. 4w+3, lane l the DK/32
+// columns from l DK/32 in all of them. Per step a lane reads its columns of k_t once from
+// shared memory (distinct addresses across the warp: no quarter-warp pass repeats another)
+// and reuses them for its four rows; delta and the gate are broadcasts. (With eight lanes
+// per row, each 16-byte read of k served four rows of a warp in four separate quarter-warp
+// passes, and the shared-memory pipe, not HBM, bounded the kernel.) Six CTAs share an SM so
+// that one's loads overlap the others' replays.
+constexpr int kDeltaRows = 32;
+
 template <int DK>
 __global__ void __launch_bounds__(256, 6)
 commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
                      const float *__restrict__ g, const float *__restrict__ delta,
                      const int *__restrict__ accepted, __half *__restrict__ state) {
-    constexpr int ROWS = 32, TPR = 8, NT = 256;
-    constexpr int NCH = DK / 8 / TPR;
+    constexpr int ROWS = kDeltaRows, RPW = ROWS / 8, CPL = DK / 32, NP = CPL / 2;
+    static_assert(CPL == 2 || CPL == 4, "two or four columns per lane");
     __shared__ __align__(16) float sk[DN_MAX_BLOCK][DK];
     __shared__ float sd[DN_MAX_BLOCK][ROWS], sg[DN_MAX_BLOCK];
     const int rblocks = DV / ROWS;
@@ -69,49 +76,68 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
     const size_t n = blockIdx.x / (rblocks * H);
     const int a = __ldg(&accepted[n % B]);
     if (a < 1 || a > T) return;  // a == 0: keep the state; out of range: ignored
-    const int tid = threadIdx.x, lr = tid / TPR, ln = tid % TPR, row = rb * ROWS + lr;
-    __half *sp = state + ((n * H + h) * (size_t)DV + row) * DK;
-    float2 s[NCH * 4];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    __half *sp = state + ((n * H + h) * (size_t)DV + rb * ROWS + warp * RPW) * DK + lane * CPL;
+
+    float2 s[RPW][NP];  // rows 4w + r, columns lane CPL + 2p, + 1
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(sp + (c * TPR + ln) * 8);
-        const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+    for (int r = 0; r < RPW; ++r) {
+        __half2 hv[NP];
+        if constexpr (NP == 2) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(sp + (size_t)r * DK);
+            hv[0] = *reinterpret_cast<const __half2 *>(&u.x);
+            hv[1] = *reinterpret_cast<const __half2 *>(&u.y);
+        } else {
+            hv[0] = *reinterpret_cast<const __half2 *>(sp + (size_t)r * DK);
+        }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
+        for (int p = 0; p < NP; ++p) s[r][p] = __half22float2(hv[p]);
     }
-    for (int i = tid; i < a * (DK / 8); i += NT) {
+    for (int i = tid; i < a * (DK / 8); i += 256) {
         const int t = i / (DK / 8), j8 = i % (DK / 8);
         float x[8];
         load8(k + ((n * T + t) * H + h) * DK + (size_t)j8 * 8, x);
-        smem_put8(sk[t], j8, x);
+        *reinterpret_cast<float4 *>(&sk[t][8 * j8]) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4 *>(&sk[t][8 * j8 + 4]) = make_float4(x[4], x[5], x[6], x[7]);
     }
-    for (int i = tid; i < a * ROWS; i += NT) {
+    for (int i = tid; i < a * ROWS; i += 256) {
         const int t = i / ROWS, r = i % ROWS;
         sd[t][r] = delta[((n * T + t) * H + h) * DV + rb * ROWS + r];
     }
     if (tid < a) sg[tid] = g[(n * T + tid) * H + h];
     __syncthreads();
     for (int t = 0; t < a; ++t) {
-        const float dt = sd[t][lr], gt = sg[t];
-        const float2 d2 = make_float2(dt, dt), g2 = make_float2(gt, gt);
-        const float4 *k4 = reinterpret_cast<const float4 *>(sk[t]);
+        const float gt = sg[t];
+        const float2 g2 = make_float2(gt, gt);
+        float2 kf[NP];
+        if constexpr (NP == 2) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(&sk[t][lane * CPL]);
+            kf[0] = make_float2(k4.x, k4.y);
+            kf[1] = make_float2(k4.z, k4.w);
+        } else {
+            kf[0] = *reinterpret_cast<const float2 *>(&sk[t][lane * CPL]);
+        }
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-            const int j8 = c * TPR + ln;
-            const float4 ka = k4[swz4(2 * j8)], kb = k4[swz4(2 * j8 + 1)];
-            s[c * 4 + 0] = __ffma2_rn(d2, make_float2(ka.x, ka.y), __fmul2_rn(g2, s[c * 4 + 0]));
-            s[c * 4 + 1] = __ffma2_rn(d2, make_float2(ka.z, ka.w), __fmul2_rn(g2, s[c * 4 + 1]));
-            s[c * 4 + 2] = __ffma2_rn(d2, make_float2(kb.x, kb.y), __fmul2_rn(g2, s[c * 4 + 2]));
-            s[c * 4 + 3] = __ffma2_rn(d2, make_float2(kb.z, kb.w), __fmul2_rn(g2, s[c * 4 + 3]));
+        for (int r = 0; r < RPW; ++r) {
+            const float dt = sd[t][warp * RPW + r];
+            const float2 d2 = make_float2(dt, dt);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) s[r][p] = __ffma2_rn(d2, kf[p], __fmul2_rn(g2, s[r][p]));
         }
     }
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-        uint4 u;
-        __half2 *hh = reinterpret_cast<__half2 *>(&u);
+    for (int r = 0; r < RPW; ++r) {
+        __half2 hv[NP];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) hh[i] = __float22half2_rn(s[c * 4 + i]);
-        *reinterpret_cast<uint4 *>(sp + (c * TPR + ln) * 8) = u;
+        for (int p = 0; p < NP; ++p) hv[p] = __float22half2_rn(s[r][p]);
+        if constexpr (NP == 2) {
+            uint2 u;
+            u.x = *reinterpret_cast<const unsigned *>(&hv[0]);
+            u.y = *reinterpret_cast<const unsigned *>(&hv[1]);
+            *reinterpret_cast<uint2 *>(sp + (size_t)r * DK) = u;
+        } else {
+            *reinterpret_cast<__half2 *>(sp + (size_t)r * DK) = hv[0];
+        }
     }
 }
 
@@ -132,8 +158,8 @@ extern "C" dn_status dn_commit_deltas(int N, int B, int H, int T, int dk, int dv
     if (!aligned(k, 16) || !aligned(state, 16) || !aligned(delta, 4) || !aligned(g, 4) ||
         !aligned(accepted_len, 4))
         return DN_ERR_INVALID_ARG;
-    if ((long long)N * H * (dv / 32) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
-    const unsigned blocks = (unsigned)((long long)N * H * (dv / 32));
+    if ((long long)N * H * (dv / kDeltaRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
+    const unsigned blocks = (unsigned)((long long)N * H * (dv / kDeltaRows));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const __half *kh = static_cast<const __half *>(k);
     __half *sh = static_cast<__half *>(state);

@@ -34,7 +34,7 @@ def main():
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--engine", choices=["mma", "tc"], default="mma", help="prefill engine")
-    ap.add_argument("--T", type=int, default=16, help="verify block width")
+    ap.add_argument("--T", type=int, default=16, help="verify block width (accept: positions per request)")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     H, d, T, V = 48, 128, a.T, 151936
@@ -48,7 +48,7 @@ def main():
             else:
                 dn.dn_commit(ckpt, acc, x["state"])
     elif a.kernel == "accept":
-        B, T4 = a.requests, 4
+        B, T4 = a.requests, a.T
         logits, target = inputs.logits_inputs(B, T4, V, dtype="f16", std=2.0, seed=2, device=dev)
         draft = inputs.draft_ids(target, inputs.accepted_lengths(B, T4, "uniform", seed=3), V)
         ws = dn.accept_workspace(B, T4, V, dev)

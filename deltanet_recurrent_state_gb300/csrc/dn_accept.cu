@@ -11,8 +11,11 @@
 // equal values, the lowest index; the order of the reduction cannot change the
 // answer. The last CTA of a row (found with a counter in the workspace) reduces
 // the row's chunk keys and writes the target id; the last row of a request then
-// computes the accepted length. Both counters are reset by the CTA that finishes
-// them, so the workspace is ready for the next call. Nothing spins or waits.
+// computes the accepted length. With few rows (a single request's verify block, or a
+// few), one level does it all: the last CTA of the whole grid reduces every row and
+// computes every accepted length, which saves the second level's fence and atomic
+// round trips on the launch's serial tail. Counters are reset by the CTA that
+// finishes them, so the workspace is ready for the next call. Nothing spins or waits.
 #include <mutex>
 
 #include <cuda_fp16.h>
@@ -26,6 +29,7 @@ namespace {
 
 constexpr int kChunk = 8192;   // vocab entries per CTA
 constexpr int kThreads = 256;
+constexpr int kFlatRows = 16;  // up to this many rows (B x T), the one-level reduction
 
 __host__ __device__ inline int accept_chunks(int V) { return (V + kChunk - 1) / kChunk; }
 
@@ -93,7 +97,8 @@ template <typename E> struct Bits;
 template <> struct Bits<unsigned short> { static constexpr int kVec = 8; };
 template <> struct Bits<unsigned int> { static constexpr int kVec = 4; };
 
-template <typename E>
+// FLAT: the one-level reduction (rows <= kFlatRows), chosen at launch.
+template <typename E, bool FLAT>
 __global__ void __launch_bounds__(kThreads)
 accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
                      const int *__restrict__ draft, int *__restrict__ target,
@@ -168,6 +173,46 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
         best = umax64(best, pack_key(order_key(rp[i]), i));
     best = block_max(best, red);
 
+    if constexpr (FLAT) {
+        const int rows = gridDim.y;
+        // One level: the last CTA of the grid reduces every row, then every request.
+        __shared__ int s_tgt[kFlatRows];
+        if (threadIdx.x == 0) {
+            ws.keys[(size_t)row * chunks + c] = best;
+            __threadfence();
+            const unsigned int prev = atomicAdd(&ws.row_count[0], 1u);
+            is_last = (prev == (unsigned int)(chunks * rows) - 1);
+        }
+        __syncthreads();
+        if (!is_last) return;
+        __threadfence();
+        const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+        for (int r = warp; r < rows; r += kThreads / 32) {
+            unsigned long long kr = 0ull;
+            for (int i = lane; i < chunks; i += 32) kr = umax64(kr, __ldcg(&ws.keys[(size_t)r * chunks + i]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) kr = umax64(kr, __shfl_xor_sync(0xffffffffu, kr, off));
+            if (lane == 0) {
+                const int t = (int)(0xffffffffu - (unsigned int)(kr & 0xffffffffull));
+                target[r] = t;
+                s_tgt[r] = t;
+            }
+        }
+        __syncthreads();
+        for (int b = warp; b < B; b += kThreads / 32) {  // accepted length = first mismatch
+            int a = T;
+            for (int t0 = 0; t0 < T && a == T; t0 += 32) {
+                const int t = t0 + lane;
+                const bool miss = t < T && __ldg(&draft[b * T + t]) != s_tgt[b * T + t];
+                const unsigned m = __ballot_sync(0xffffffffu, miss);
+                if (m) a = t0 + __ffs(m) - 1;
+            }
+            if (lane == 0) accepted[b] = a;
+        }
+        if (threadIdx.x == 0) ws.row_count[0] = 0u;
+        return;
+    }
+
     if (threadIdx.x == 0) {
         ws.keys[(size_t)row * chunks + c] = best;
         __threadfence();
@@ -212,6 +257,26 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
     }
 }
 
+template <typename E, bool FLAT>
+void launch_accept_as(int B, int T, int V, const void *logits, const int32_t *draft, int32_t *target,
+                      int32_t *accepted, const AcceptWorkspace &ws, cudaStream_t st) {
+    const dim3 grid(accept_chunks(V), B * T);
+    accept_greedy_kernel<E, FLAT><<<grid, kThreads, 0, st>>>(B, T, V, static_cast<const E *>(logits), draft,
+                                                             target, accepted, ws);
+}
+
+void launch_accept(int B, int T, int V, dn_dtype logit_dt, const void *logits, const int32_t *draft,
+                   int32_t *target, int32_t *accepted, const AcceptWorkspace &ws, cudaStream_t st) {
+    const bool flat = B * T <= kFlatRows;
+    if (logit_dt == DN_F16) {
+        if (flat) launch_accept_as<unsigned short, true>(B, T, V, logits, draft, target, accepted, ws, st);
+        else launch_accept_as<unsigned short, false>(B, T, V, logits, draft, target, accepted, ws, st);
+    } else {
+        if (flat) launch_accept_as<unsigned int, true>(B, T, V, logits, draft, target, accepted, ws, st);
+        else launch_accept_as<unsigned int, false>(B, T, V, logits, draft, target, accepted, ws, st);
+    }
+}
+
 }  // namespace
 }  // namespace dn
 
@@ -234,16 +299,8 @@ extern "C" dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, co
         return DN_ERR_INVALID_ARG;
     if (workspace_bytes < accept_ws_bytes(B, T, V)) return DN_ERR_INVALID_ARG;
     const AcceptWorkspace ws = accept_ws(workspace, B, T, V);
-    const dim3 grid(accept_chunks(V), B * T);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (logit_dt == DN_F16)
-        accept_greedy_kernel<unsigned short><<<grid, kThreads, 0, st>>>(
-            B, T, V, static_cast<const unsigned short *>(logits), draft_ids, target_ids,
-            accepted_len, ws);
-    else
-        accept_greedy_kernel<unsigned int><<<grid, kThreads, 0, st>>>(
-            B, T, V, static_cast<const unsigned int *>(logits), draft_ids, target_ids,
-            accepted_len, ws);
+    launch_accept(B, T, V, logit_dt, logits, draft_ids, target_ids, accepted_len, ws, st);
     return launch_status();
 }
 
@@ -308,14 +365,6 @@ extern "C" dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logi
         cudaGetLastError();
         return DN_ERR_CUDA;
     }
-    const dim3 grid(accept_chunks(V), B * T);
-    if (logit_dt == DN_F16)
-        accept_greedy_kernel<unsigned short><<<grid, kThreads, 0, st>>>(
-            B, T, V, static_cast<const unsigned short *>(logits), draft_ids, target_ids,
-            accepted_len, ws);
-    else
-        accept_greedy_kernel<unsigned int><<<grid, kThreads, 0, st>>>(
-            B, T, V, static_cast<const unsigned int *>(logits), draft_ids, target_ids,
-            accepted_len, ws);
+    launch_accept(B, T, V, logit_dt, logits, draft_ids, target_ids, accepted_len, ws, st);
     return launch_status();
 }

@@ -156,19 +156,22 @@ __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
 // (dn_verify_block_deltas), from which dn_commit_deltas rebuilds the accepted state.
 // TM: the block capacity the shared tiles are sized for (16, or 8 for blocks of up to 8
 // tokens, whose smaller tiles let more CTAs share an SM).
-template <int DK, bool CKPT, int TM>
-__global__ void __launch_bounds__(256, TM == 8 ? 6 : 5)
+// ROWS: the state rows of a CTA (32, or 64 so that the head's state-independent work -- the
+// k/q tiles, the grams, L and M, the gate scan -- is shared by twice the rows).
+static_assert(DN_MAX_BLOCK == 16, "tile capacities 8 and 16");
+template <int DK, bool CKPT, int TM, int ROWS>
+__global__ void __launch_bounds__(256, ROWS == 64 ? 4 : (TM == 8 ? 6 : 5))
 verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
                  const __half *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ g, const __half *__restrict__ s_in,
                  __half *__restrict__ out, __half *__restrict__ ckpt, float *__restrict__ delta) {
-    constexpr int ROWS = 32, TPR = 8, NT = 256;
+    constexpr int NT = 256, TPR = NT / ROWS;  // threads per state row
     constexpr int CPR = DK / 8;        // 16-byte chunks per row
     constexpr int NCH = CPR / TPR;     // chunks per lane
     constexpr int KS = DK / 16;        // MMA k-steps
     __shared__ __align__(128) uint4 sS0[ROWS * CPR];
     __shared__ __align__(128) uint4 sKQ[2 * TM * CPR];  // rows 0..TM-1 k_t, TM..2TM-1 q_t
-    __shared__ __align__(16) float sk[TM][DK];           // k_t in fp32 (swz4)
+    __shared__ __align__(16) float sk[CKPT ? TM : 1][DK];  // k_t in fp32 (swz4), for the checkpoint update
     __shared__ float proj[ROWS][2 * TM + 1];              // [row][t] S0 k_t, [row][TM+t] S0 q_t
     __shared__ float gram[2 * TM][TM + 1];                // [t][s] k_t.k_s, [TM+t][s] q_t.k_s
     __shared__ float sL[TM][TM], sM[TM][TM];
@@ -204,15 +207,19 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             const size_t off = ((n * T + t) * H + h) * DK + (size_t)j * 8;
             uk = *reinterpret_cast<const uint4 *>(k + off);
             uq = *reinterpret_cast<const uint4 *>(q + off);
-            float x[8];
-            const __half2 *h2 = reinterpret_cast<const __half2 *>(&uk);
+        }
+        if constexpr (CKPT) {
+            if (t < T) {
+                float x[8];
+                const __half2 *h2 = reinterpret_cast<const __half2 *>(&uk);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(h2[e]);
-                x[2 * e] = f.x;
-                x[2 * e + 1] = f.y;
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(h2[e]);
+                    x[2 * e] = f.x;
+                    x[2 * e + 1] = f.y;
+                }
+                smem_put8(sk[t], j, x);
             }
-            smem_put8(sk[t], j, x);
         }
         sKQ[hsw<CPR>(t, j)] = uk;
         sKQ[hsw<CPR>(TM + t, j)] = uq;
@@ -243,10 +250,9 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     }
     __syncthreads();
 
-    // 2. proj = S0 [K;Q]^T (one 16x8 tile per warp); gram = [K;Q] K^T (one tile per warp)
+    // 2. proj = S0 [K;Q]^T in 16x8 tiles; gram = [K;Q] K^T (one tile per warp)
     constexpr int NG = TM / 8, MG = 2 * TM / 16;  // gram tiles: n (tokens of K), m (rows of [K;Q])
-    if ((warp & 3) * 8 < 2 * TM) {
-        const int mt = warp >> 2, nt = warp & 3;
+    auto proj_tile = [&](int mt, int nt) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -260,22 +266,31 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         proj[r0][c0 + 1] = d[1];
         proj[r0 + 8][c0] = d[2];
         proj[r0 + 8][c0 + 1] = d[3];
-        if (warp < MG * NG) {
-            const int gm = warp / NG, gn = warp % NG;
-            float e[4] = {0.f, 0.f, 0.f, 0.f};
+    };
+    auto gram_tile = [&](int gm, int gn) {
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                unsigned a[4], b[2];
-                ldsm_x4(a, &sKQ[hsw<CPR>(gm * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
-                ldsm_x2(b, &sKQ[hsw<CPR>(gn * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
-                mma_16816(e, a, b);
-            }
-            const int g0 = gm * 16 + (lane >> 2), h0 = gn * 8 + 2 * (lane & 3);
-            gram[g0][h0] = e[0];
-            gram[g0][h0 + 1] = e[1];
-            gram[g0 + 8][h0] = e[2];
-            gram[g0 + 8][h0 + 1] = e[3];
+        for (int ks = 0; ks < KS; ++ks) {
+            unsigned a[4], b[2];
+            ldsm_x4(a, &sKQ[hsw<CPR>(gm * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+            ldsm_x2(b, &sKQ[hsw<CPR>(gn * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+            mma_16816(e, a, b);
         }
+        const int g0 = gm * 16 + (lane >> 2), h0 = gn * 8 + 2 * (lane & 3);
+        gram[g0][h0] = e[0];
+        gram[g0][h0 + 1] = e[1];
+        gram[g0 + 8][h0] = e[2];
+        gram[g0 + 8][h0 + 1] = e[3];
+    };
+    if constexpr (ROWS == 32) {  // warp = (m tile) * 4 + (n tile)
+        if ((warp & 3) * 8 < 2 * TM) {
+            proj_tile(warp >> 2, warp & 3);
+            if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
+        }
+    } else {
+        constexpr int PN = 2 * TM / 8, PTILES = (ROWS / 16) * PN;
+        for (int tile = warp; tile < PTILES; tile += NT / 32) proj_tile(tile / PN, tile % PN);
+        if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
     }
     __syncthreads();
 
@@ -289,7 +304,8 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     __syncthreads();
 
     // 4. delta_t by forward substitution, one lane per row
-    if (warp == 0) {
+    if (warp < ROWS / 32) {
+        const int rl = warp * 32 + lane;  // the row of this lane
         float dl[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) {
@@ -298,8 +314,8 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
                 float acc = 0.f;
 #pragma unroll
                 for (int s2 = 0; s2 < t; ++s2) acc = fmaf(sL[t][s2], dl[s2], acc);
-                dl[t] = sbeta[t] * (sv[t][lane] - sgam[t] * proj[lane][t] - acc);
-                sd[t][lane] = dl[t];
+                dl[t] = sbeta[t] * (sv[t][rl] - sgam[t] * proj[rl][t] - acc);
+                sd[t][rl] = dl[t];
             }
         }
     }
@@ -348,6 +364,21 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
 constexpr int kRows = 32;
 constexpr int kTpr = 8;
 
+// State rows per CTA of verify_wy_kernel. With checkpoints, 32: the rows' state lives in
+// registers for the update, and 64-row CTAs measured slower (fewer CTAs per SM, spills at
+// T = 16). Writing deltas, 64: no state in registers, and the head's state-independent work
+// is shared by twice the rows (a whole head per CTA measured slower again).
+constexpr int kWyRowsCkpt = 32, kWyRowsDelta = 64;
+
+template <int DK, bool CKPT, int TM>
+void launch_verify_wy(int N, int H, int T, int dv, const __half *q, const __half *k, const __half *v,
+                      const float *beta, const float *g, const __half *s_in, __half *out, __half *ckpt,
+                      float *delta, cudaStream_t st) {
+    constexpr int R = CKPT ? kWyRowsCkpt : kWyRowsDelta;  // dv (64 or 128) is a multiple of both
+    const unsigned blocks = (unsigned)((long long)N * H * (dv / R));
+    verify_wy_kernel<DK, CKPT, TM, R><<<blocks, 256, 0, st>>>(H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta);
+}
+
 template <int DK, typename IO, typename ST>
 void launch_verify(int N, int H, int T, int dv, const void *q, const void *k, const void *v,
                    const float *beta, const float *g, const void *s_in, void *out, void *ckpt,
@@ -380,18 +411,17 @@ extern "C" dn_status dn_verify_block(int N, int H, int T, int dk, int dv, dn_dty
     if ((long long)N * H * (dv / kRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (io_dt == DN_F16) {
-        const unsigned blocks = (unsigned)((long long)N * H * (dv / kRows));
         const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
         const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
         __half *oh = static_cast<__half *>(out), *ch = static_cast<__half *>(ckpt);
         if (dk == 128 && T <= 8)
-            verify_wy_kernel<128, true, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+            launch_verify_wy<128, true, 8>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr, st);
         else if (dk == 128)
-            verify_wy_kernel<128, true, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+            launch_verify_wy<128, true, kMaxT>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr, st);
         else if (T <= 8)
-            verify_wy_kernel<64, true, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+            launch_verify_wy<64, true, 8>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr, st);
         else
-            verify_wy_kernel<64, true, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr);
+            launch_verify_wy<64, true, kMaxT>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, ch, nullptr, st);
     } else {
         if (dk == 128) launch_verify<128, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
         else launch_verify<64, float, float>(N, H, T, dv, q, k, v, beta, g, state_in, out, ckpt, st);
@@ -416,17 +446,16 @@ extern "C" dn_status dn_verify_block_deltas(int N, int H, int T, int dk, int dv,
         return DN_ERR_INVALID_ARG;
     if ((long long)N * H * (dv / kRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const unsigned blocks = (unsigned)((long long)N * H * (dv / kRows));
     const __half *qh = static_cast<const __half *>(q), *kh = static_cast<const __half *>(k);
     const __half *vh = static_cast<const __half *>(v), *sh = static_cast<const __half *>(state_in);
     __half *oh = static_cast<__half *>(out);
     if (dk == 128 && T <= 8)
-        verify_wy_kernel<128, false, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+        launch_verify_wy<128, false, 8>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta, st);
     else if (dk == 128)
-        verify_wy_kernel<128, false, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+        launch_verify_wy<128, false, kMaxT>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta, st);
     else if (T <= 8)
-        verify_wy_kernel<64, false, 8><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+        launch_verify_wy<64, false, 8>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta, st);
     else
-        verify_wy_kernel<64, false, kMaxT><<<blocks, 256, 0, st>>>(H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta);
+        launch_verify_wy<64, false, kMaxT>(N, H, T, dv, qh, kh, vh, beta, g, sh, oh, nullptr, delta, st);
     return launch_status();
 }

@@ -70,7 +70,9 @@ def test_negative_values_and_extremes_fp16(cuda):
     _check(logits, torch.zeros((2, 3), dtype=torch.int32), cuda)
 
 
-@pytest.mark.parametrize("B,T", [(1, 1), (1, 16), (64, 4), (7, 3)])
+# B x T up to 16 rows take the one-level reduction (the grid's last CTA finishes every row and
+# request), more rows the two-level one; (2, 8) and (17, 1) sit on either side of that line.
+@pytest.mark.parametrize("B,T", [(1, 1), (1, 16), (2, 8), (17, 1), (64, 4), (7, 3)])
 def test_planted_prefix_lengths(B, T, cuda):
     V = 151936
     logits, target = inputs.logits_inputs(B, T, V, dtype="f16", std=2.0, seed=B * 100 + T)
@@ -80,9 +82,11 @@ def test_planted_prefix_lengths(B, T, cuda):
     np.testing.assert_array_equal(acc_ref, a.numpy())
 
 
-def test_workspace_reused_across_calls(cuda):
-    # the counters reset themselves: the same workspace serves many calls in a row
-    B, T, V = 5, 4, 30000
+@pytest.mark.parametrize("B,T", [(5, 4), (4, 4), (1, 17)])
+def test_workspace_reused_across_calls(B, T, cuda):
+    # the counters reset themselves: the same workspace serves many calls in a row (both the
+    # one-level reduction, 16 rows, and the two-level one)
+    V = 30000
     ws = dn.accept_workspace(B, T, V, cuda)
     for s in range(6):
         logits, target = inputs.logits_inputs(B, T, V, dtype="f32", std=1.0, seed=50 + s)

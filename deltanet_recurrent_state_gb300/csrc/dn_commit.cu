@@ -52,17 +52,18 @@ commit_kernel(int B, int T, size_t set_bytes, const uint4 *__restrict__ ckpt,
 // S_a = g_{a-1} ( ... (g_0 S_0 + delta_0 k_0^T) ... ) + delta_{a-1} k_{a-1}^T, applied here
 // to the old state in place with exactly the arithmetic (packed fp32x2 FMAs in the same
 // order) the checkpoint path uses, so both paths commit bit-identical states.
-// A CTA owns 32 rows of one (state set, head): warp w the rows 4w .. 4w+3, lane l the DK/32
+// A CTA owns 64 rows of one (state set, head): warp w the rows 8w .. 8w+7, lane l the DK/32
 // columns from l DK/32 in all of them. Per step a lane reads its columns of k_t once from
 // shared memory (distinct addresses across the warp: no quarter-warp pass repeats another)
-// and reuses them for its four rows; delta and the gate are broadcasts. (With eight lanes
+// and reuses them for its eight rows; delta and the gate are broadcasts. (With eight lanes
 // per row, each 16-byte read of k served four rows of a warp in four separate quarter-warp
-// passes, and the shared-memory pipe, not HBM, bounded the kernel.) Six CTAs share an SM so
-// that one's loads overlap the others' replays.
-constexpr int kDeltaRows = 32;
+// passes, and the shared-memory pipe, not HBM, bounded the kernel; with four rows per warp
+// the shared reads and loop overhead, not the packed FMAs, still made up most of the
+// instructions.)
+constexpr int kDeltaRows = 64;
 
 template <int DK>
-__global__ void __launch_bounds__(256, 6)
+__global__ void __launch_bounds__(256, 4)
 commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
                      const float *__restrict__ g, const float *__restrict__ delta,
                      const int *__restrict__ accepted, __half *__restrict__ state) {

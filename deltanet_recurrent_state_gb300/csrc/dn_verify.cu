@@ -138,7 +138,8 @@ verify_block_kernel(int H, int T, int DV, const IO *__restrict__ q, const IO *__
 //   3. L, M and Gamma (16 x 16 per head) from gram and the gates;
 //   4. one lane per row solves delta_t by forward substitution;
 //   5. every lane applies S_t = g_t S_{t-1} + delta_t k_t^T to its 16 fp32 state
-//      elements with packed fp32x2 FMAs and streams the fp16 checkpoint;
+//      elements with packed fp32x2 FMAs, reading k_t from the fp16 tile of step 1 (one
+//      16-byte read per 8 elements; fp16 -> fp32 is exact), and streams the fp16 checkpoint;
 //   6. o_t from proj, M and delta.
 // The contraction is a few dozen m16n8k16 MMAs per CTA; its job is to remove the
 // two per-token dot products (two FMAs per state element per token) from the
@@ -171,7 +172,6 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     constexpr int KS = DK / 16;        // MMA k-steps
     __shared__ __align__(128) uint4 sS0[ROWS * CPR];
     __shared__ __align__(128) uint4 sKQ[2 * TM * CPR];  // rows 0..TM-1 k_t, TM..2TM-1 q_t
-    __shared__ __align__(16) float sk[CKPT ? TM : 1][DK];  // k_t in fp32 (swz4), for the checkpoint update
     __shared__ float proj[ROWS][2 * TM + 1];              // [row][t] S0 k_t, [row][TM+t] S0 q_t
     __shared__ float gram[2 * TM][TM + 1];                // [t][s] k_t.k_s, [TM+t][s] q_t.k_s
     __shared__ float sL[TM][TM], sM[TM][TM];
@@ -207,19 +207,6 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             const size_t off = ((n * T + t) * H + h) * DK + (size_t)j * 8;
             uk = *reinterpret_cast<const uint4 *>(k + off);
             uq = *reinterpret_cast<const uint4 *>(q + off);
-        }
-        if constexpr (CKPT) {
-            if (t < T) {
-                float x[8];
-                const __half2 *h2 = reinterpret_cast<const __half2 *>(&uk);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(h2[e]);
-                    x[2 * e] = f.x;
-                    x[2 * e + 1] = f.y;
-                }
-                smem_put8(sk[t], j, x);
-            }
         }
         sKQ[hsw<CPR>(t, j)] = uk;
         sKQ[hsw<CPR>(TM + t, j)] = uq;
@@ -333,15 +320,13 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     for (int t = 0; CKPT && t < T; ++t) {
         const float dt = sd[t][lr], gt = sg[t];
         const float2 d2 = make_float2(dt, dt), g2 = make_float2(gt, gt);
-        const float4 *k4 = reinterpret_cast<const float4 *>(sk[t]);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-            const int j8 = c * TPR + ln;
-            const float4 ka = k4[swz4(2 * j8)], kb = k4[swz4(2 * j8 + 1)];
-            s[c * 4 + 0] = __ffma2_rn(d2, make_float2(ka.x, ka.y), __fmul2_rn(g2, s[c * 4 + 0]));
-            s[c * 4 + 1] = __ffma2_rn(d2, make_float2(ka.z, ka.w), __fmul2_rn(g2, s[c * 4 + 1]));
-            s[c * 4 + 2] = __ffma2_rn(d2, make_float2(kb.x, kb.y), __fmul2_rn(g2, s[c * 4 + 2]));
-            s[c * 4 + 3] = __ffma2_rn(d2, make_float2(kb.z, kb.w), __fmul2_rn(g2, s[c * 4 + 3]));
+            const uint4 ku = sKQ[hsw<CPR>(t, c * TPR + ln)];  // k_t, 8 fp16 values (exact in fp32)
+            const __half2 *kh = reinterpret_cast<const __half2 *>(&ku);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                s[c * 4 + i] = __ffma2_rn(d2, __half22float2(kh[i]), __fmul2_rn(g2, s[c * 4 + i]));
             __stcs(reinterpret_cast<uint4 *>(dst + c * TPR * 8), pack8_half2(&s[c * 4]));
         }
         dst += tstride;

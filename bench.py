@@ -291,61 +291,101 @@ def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True)
     return secs, per, (t_wall0, t_wall1)
 
 
-def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True):
+def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
     """The same step through the public API with host inputs: every step copies its
     inputs from pinned host memory and reads its results back (the target ids and the
     accepted length, which a serving loop needs to emit tokens; the outputs o feed the
-    next sub-layer on the device), and the host waits for them before the next step. A step's
-    inputs sit in one pinned buffer and its results in one device region (the tensors the
-    calls take are views of them), so each direction is a single copy.
-    With `graphs`, each buffer set's step (its host-to-device copies, the three calls
-    and the device-to-host copies, all issued through the public binding) is captured
-    once in a CUDA graph, and a step is one replay; otherwise every call is issued from
-    Python each step. Returns (seconds, h2d bytes per step, d2h bytes per step)."""
+    next sub-layer on the device), and the host waits for them before the next step.
+    A step's inputs sit in one pinned buffer and its results in one device region (the
+    tensors the calls take are views of them).
+    `groups` is a count of equal groups or a list of group sizes (state sets per group). With
+    one group the inputs go over in a single copy before the three calls. With more the step
+    is pipelined over the layers: the state sets split into contiguous groups, each
+    group's q, k, v, beta and g are one contiguous piece of the
+    pinned buffer and go over in their own copy on a copy stream, and the group's verify
+    (dn_verify_block on that slice of the state sets) starts on the compute stream as soon
+    as its copy has landed, so the host link carries the later groups while the earlier
+    ones verify. The logits and draft ids go last; accept and commit follow as before.
+    With `graphs`, each buffer set's step (the copies, the calls and the device-to-host
+    copy, all issued through the public binding) is captured once in a CUDA graph, and a
+    step is one replay; otherwise every call is issued from Python each step. Returns
+    (seconds, h2d bytes per step, d2h bytes per step)."""
     import torch
     from deltanet_recurrent_state_gb300 import binding as dn
-    in_keys = ("q", "k", "v", "beta", "g", "logits", "draft")
+    L = sets[0]["q"].shape[0]
+    if isinstance(groups, int):
+        assert L % groups == 0, "layers must split evenly into the groups"
+        sizes = [L // groups] * groups
+    else:
+        sizes = list(groups)
+    assert sum(sizes) == L and min(sizes) > 0
+    bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
+    groups = len(sizes)
+    group_keys = ("q", "k", "v", "beta", "g")
+    tail_keys = ("logits", "draft")
     out_keys = ("tgt", "acc")  # what the serving loop needs back; o stays on the device
 
-    def packed(x, keys, pinned):
-        """One byte buffer holding the tensors `keys` of x (256-byte aligned), and views of
-        it with their shapes and dtypes."""
+    def entries_in(x):
+        e = [("%s%d" % (k, gi), x[k][bounds[gi]:bounds[gi + 1]]) for gi in range(groups) for k in group_keys]
+        return e + [(k, x[k]) for k in tail_keys]
+
+    def packed(entries, pinned):
+        """One byte buffer holding the tensors of `entries` in order (256-byte aligned),
+        views of it with their shapes and dtypes, and each entry's byte offset."""
         offs, total = {}, 0
-        for k in keys:
-            offs[k] = total
-            total += (x[k].numel() * x[k].element_size() + 255) // 256 * 256
+        for name, t in entries:
+            offs[name] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
         buf = torch.empty(total, dtype=torch.uint8, pin_memory=pinned) if pinned else \
             torch.empty(total, dtype=torch.uint8, device=device)
-        views = {k: buf[offs[k]:offs[k] + x[k].numel() * x[k].element_size()].view(x[k].dtype)
-                 .view(x[k].shape) for k in keys}
-        return buf, views
+        views = {name: buf[offs[name]:offs[name] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for name, t in entries}
+        return buf, views, offs, total
 
-    # per buffer set: device inputs and results as views of one region each, so a step is
-    # one host-to-device and one device-to-host copy
-    host, dev_in, dev_out, host_out = [], [], [], []
+    host, dev_in, dev_out, host_out, segs = [], [], [], [], None
     for x in sets:
-        hb, hv = packed(x, in_keys, True)
-        db, dv_ = packed(x, in_keys, False)
-        for k in in_keys:
-            hv[k].copy_(x[k].cpu())
-            dv_[k].copy_(x[k])
-        ob, ov = packed(x, out_keys, False)
-        hob, hov = packed(x, out_keys, True)
+        ent = entries_in(x)
+        hb, hv, offs, total = packed(ent, True)
+        db, dv_, _, _ = packed(ent, False)
+        for name, t in ent:
+            hv[name].copy_(t.cpu())
+            dv_[name].copy_(t)
+        outs = [(k, x[k]) for k in out_keys]
+        ob, ov, _, _ = packed(outs, False)
+        hob, _, _, _ = packed(outs, True)
         host.append(hb)
         dev_in.append((db, dv_))
         dev_out.append((ob, ov))
         host_out.append(hob)
+        # byte ranges copied one by one: each group's inputs, then the logits and drafts
+        starts = [offs["q%d" % gi] for gi in range(groups)] + [offs["logits"]]
+        segs = [(starts[i], starts[i + 1]) for i in range(groups)] + [(offs["logits"], total)]
     h2d = host[0].numel()
     d2h = host_out[0].numel()
+    copy_stream = torch.cuda.Stream(device=device)
+    events = [[torch.cuda.Event() for _ in range(groups + 1)] for _ in sets]
 
     def body(j):
         x = dict(sets[j])
-        x.update(dev_in[j][1])
+        dvw = dev_in[j][1]
         x.update(dev_out[j][1])
-        dev_in[j][0].copy_(host[j], non_blocking=True)  # one pinned copy (the host link's full rate)
-        dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
-                           x["ckpt"], stream=stream)
-        dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+        if groups == 1:
+            dev_in[j][0].copy_(host[j], non_blocking=True)  # one pinned copy (the host link's full rate)
+        else:
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for i, (a0, a1) in enumerate(segs):
+                    dev_in[j][0][a0:a1].copy_(host[j][a0:a1], non_blocking=True)
+                    events[j][i].record(copy_stream)
+        for gi in range(groups):
+            if groups > 1:
+                stream.wait_event(events[j][gi])
+            sl = slice(bounds[gi], bounds[gi + 1])
+            dn.dn_verify_block(dvw["q%d" % gi], dvw["k%d" % gi], dvw["v%d" % gi], dvw["beta%d" % gi],
+                               dvw["g%d" % gi], x["state"][sl], x["out"][sl], x["ckpt"][sl], stream=stream)
+        if groups > 1:
+            stream.wait_event(events[j][groups])
+        dn.dn_accept_greedy(dvw["logits"], dvw["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
         dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
         host_out[j].copy_(dev_out[j][0], non_blocking=True)
 
@@ -722,9 +762,15 @@ def main():
     value = units_per_rank * world / secs
 
     e2e_k = max(3, min(args.steps, 200))
-    e2e_s, h2d, d2h = e2e_steps(w, sets, e2e_k, 3, stream, device)
+    # layer groups of the pipelined step, growing (48 layers: 8, 16, 24): the first group's
+    # copy is short so the verify starts early, and each later copy lands before the verify
+    # of the groups before it ends (copies move a layer in ~3.4 us, verify takes ~4.3 us)
+    L6 = w["L"] // 6
+    e2e_groups = (L6, 2 * L6, w["L"] - 3 * L6)
+    e2e_s, h2d, d2h = e2e_steps(w, sets, e2e_k, 3, stream, device, groups=e2e_groups)
     e2e_value = B * T * w["L"] * e2e_k / e2e_s
-    e2e_eager_s, _, _ = e2e_steps(w, sets, e2e_k, 3, stream, device, graphs=False)
+    e2e_eager_s, _, _ = e2e_steps(w, sets, e2e_k, 3, stream, device, graphs=False, groups=e2e_groups)
+    e2e_serial_s, _, _ = e2e_steps(w, sets, e2e_k, 3, stream, device, groups=1)
 
     rows = {}
     if not args.no_rows and rank == 0:
@@ -789,10 +835,14 @@ def main():
         },
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_k,
-                "how": "one CUDA graph replay per step (one host-to-device copy of the packed "
-                       "inputs, the three calls, device-to-host target ids and accepted length); "
-                       "the host waits for each step's results",
-                "eager_value": B * T * w["L"] * e2e_k / e2e_eager_s},
+                "how": "one CUDA graph replay per step: the inputs of layer groups of %s layers go "
+                       "over in one copy each on a copy stream, each group's verify starts when its "
+                       "copy has landed, then the logits and drafts, accept, commit and the "
+                       "device-to-host read of the target ids and accepted length; the host waits "
+                       "for each step's results" % "/".join(str(x) for x in e2e_groups),
+                "eager_value": B * T * w["L"] * e2e_k / e2e_eager_s,
+                "serial_value": B * T * w["L"] * e2e_k / e2e_serial_s,
+                "serial_how": "the same step with all inputs in one copy before the three calls"},
         "gpu_launches": 3 * args.steps,
         "clocks": clock_info,
         "cpu_baseline": cpu,

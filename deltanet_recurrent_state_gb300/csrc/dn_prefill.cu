@@ -198,8 +198,8 @@ __device__ __forceinline__ int box_chunk(int rows, int r, int ch) {
 // there are fewer (sequence, head) pairs than SMs (each half then repeats the
 // state-independent work, which idle SMs absorb).
 // Warp roles. Chain warps (DVC/16 of them, 16 dv-rows each) hold the state and run
-// the state-dependent steps of chunk c; four prep warps meanwhile load chunk c+1 and
-// compute its state-independent products. Hand-off per chunk parity p with named
+// the state-dependent steps of chunk c; four prep warps meanwhile fetch chunk c+1's gates
+// and compute its state-independent products. Hand-off per chunk parity p with named
 // barriers over all threads: FULL[p] (prep arrives, chain waits) when chunk c's
 // inputs and products are ready, EMPTY[p] (chain arrives, prep waits) when the
 // chain is done with them. Inputs are triple buffered (chunk c, chunk c+1 and the
@@ -238,8 +238,10 @@ template <int N>
 __device__ __forceinline__ void regs_lower() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
 // 16-row state tiles per chain warp. Two tiles per warp halve the operand fragments each
-// warp loads from shared memory but measure no faster on GB300 (the chain is bound by the
-// latency of its dependent steps, not by shared-memory bandwidth), so one it is.
+// warp loads from shared memory (which runs at about 80 % of its throughput here), but they
+// leave one chain warp per scheduler instead of two and need 128 fp32 state registers a
+// thread; even with the chain warpgroup raised to 232 registers they measure slower, so one
+// it is.
 constexpr int kRowTiles = 1;
 
 // Count of prefill input waits that ran out (read by dn_prefill_wait_timeouts).

@@ -291,6 +291,20 @@ def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True)
     return secs, per, (t_wall0, t_wall1)
 
 
+def e2e_group_bounds(L, groups):
+    """State-set boundaries [0, ..., L] of the end-to-end step's layer groups: `groups` is
+    a count of equal groups or a list of group sizes."""
+    if isinstance(groups, int):
+        if groups < 1 or L % groups != 0:
+            raise ValueError("%d layers do not split into %d equal groups" % (L, groups))
+        sizes = [L // groups] * groups
+    else:
+        sizes = [int(x) for x in groups]
+    if not sizes or min(sizes) < 1 or sum(sizes) != L:
+        raise ValueError("group sizes %s do not cover %d layers" % (sizes, L))
+    return [sum(sizes[:i]) for i in range(len(sizes) + 1)]
+
+
 def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
     """The same step through the public API with host inputs: every step copies its
     inputs from pinned host memory and reads its results back (the target ids and the
@@ -312,15 +326,8 @@ def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
     (seconds, h2d bytes per step, d2h bytes per step)."""
     import torch
     from deltanet_recurrent_state_gb300 import binding as dn
-    L = sets[0]["q"].shape[0]
-    if isinstance(groups, int):
-        assert L % groups == 0, "layers must split evenly into the groups"
-        sizes = [L // groups] * groups
-    else:
-        sizes = list(groups)
-    assert sum(sizes) == L and min(sizes) > 0
-    bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
-    groups = len(sizes)
+    bounds = e2e_group_bounds(sets[0]["q"].shape[0], groups)
+    groups = len(bounds) - 1
     group_keys = ("q", "k", "v", "beta", "g")
     tail_keys = ("logits", "draft")
     out_keys = ("tgt", "acc")  # what the serving loop needs back; o stays on the device

@@ -99,3 +99,13 @@ def test_context_bytes():
     # every token once, plus length in and (drafts, count, match length) out per request
     assert bench.context_bytes([26000], 8) == 26000 * 4 + 4 * (1 + 8 + 2)
     assert bench.context_bytes([10, 0], 4) == 40 + 2 * 4 * 7
+
+
+def test_e2e_group_bounds():
+    # the end-to-end step's layer groups: equal counts or explicit growing sizes
+    assert bench.e2e_group_bounds(48, 1) == [0, 48]
+    assert bench.e2e_group_bounds(48, 4) == [0, 12, 24, 36, 48]
+    assert bench.e2e_group_bounds(48, (8, 16, 24)) == [0, 8, 24, 48]
+    for bad in (5, 0, (8, 16), (8, 16, 25), (0, 24, 24)):
+        with pytest.raises(ValueError):
+            bench.e2e_group_bounds(48, bad)

@@ -36,6 +36,7 @@ SIGNATURES = {
     "dn_status_string": (ctypes.c_char_p, [_I]),
     "dn_accept_greedy_noalloc": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "dn_prefill_wait_timeouts": (ctypes.c_uint, []),
+    "dn_wait_selftest": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "dn_verify_block_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "dn_commit_deltas": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "dn_prefix_cache_create": (_P, [_I, _I]),
@@ -237,6 +238,14 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
 
 def dn_prefill_wait_timeouts():
     return int(load_library().dn_prefill_wait_timeouts())
+
+
+def dn_wait_selftest(tries, device=None, stream=None):
+    """Runs the bounded-wait self-test; returns (gave_up_unfinished, returned_finished)."""
+    result = torch.full((2,), -1, dtype=torch.int32, device=device or "cuda")
+    _check("dn_wait_selftest", load_library().dn_wait_selftest(int(tries), result.data_ptr(), _stream(stream)))
+    torch.cuda.synchronize(result.device)
+    return int(result[0]), int(result[1])
 
 
 def dn_context_drafts(context, lengths, n_max=4, n_min=1, K=8, drafts=None, count=None,

@@ -367,6 +367,18 @@ int dn_prefix_cache_size(dn_prefix_cache *c);
  */
 unsigned int dn_prefill_wait_timeouts(void);
 
+/*
+ * dn_wait_selftest -- checks on the device the bounded wait the prefill kernels use.
+ *
+ * Launches one small kernel on `stream` that waits, with at most `tries` polls, on a
+ * shared-memory barrier nothing has arrived on, then arrives once and waits again.
+ * Writes result[0] = 1 if the first wait gave up (as it must), result[1] = 1 if the
+ * second returned (as it must). result: 2 int32 in device memory, 4-byte aligned, owned by
+ * the caller. 1 <= tries <= 2^20 (the kernel ends within microseconds at 1000 polls).
+ * Errors: DN_ERR_INVALID_ARG (nothing launched), DN_ERR_CUDA (launch failed).
+ */
+dn_status dn_wait_selftest(int tries, int32_t *result, dn_stream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *dn_status_string(dn_status s);
 

@@ -173,3 +173,18 @@ def test_tc_engine_full_size_layer_sampled(cuda):
     assert_close("out", out[:, :, heads], ref[0], TOL["f16"])
     assert_close("ckpt", ckpt[:, :, heads], ref[1], TOL["f16"])
     assert_close("state_out", s_out[:, heads], ref[2], TOL["f16"])
+
+
+@pytest.mark.parametrize("tries", [1, 1000])
+def test_bounded_wait_gives_up_and_reports(tries, cuda):
+    # the prefill kernels' input waits are bounded: on a barrier nothing arrives on, the wait
+    # runs out after `tries` polls and reports it; after the arrival the same wait returns
+    assert dn.dn_wait_selftest(tries, device=cuda) == (1, 1)
+
+
+def test_wait_selftest_rejects_bad_arguments(cuda):
+    lib = dn.load_library()
+    buf = torch.zeros(2, dtype=torch.int32, device=cuda)
+    assert lib.dn_wait_selftest(0, buf.data_ptr(), None) == 1          # DN_ERR_INVALID_ARG
+    assert lib.dn_wait_selftest((1 << 20) + 1, buf.data_ptr(), None) == 1
+    assert lib.dn_wait_selftest(10, None, None) == 1

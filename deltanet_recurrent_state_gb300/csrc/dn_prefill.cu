@@ -216,21 +216,27 @@ constexpr int kPrepThreads = 128, kProducerThreads = 32;
 
 // A thirteenth warp caps every thread of the CTA at 128 registers: the register file is
 // split between the SM's four schedulers, and one of them then holds four warps. The chain
-// warps of a dk = 128 state over 128 rows want about 157 and measure slower squeezed, so
-// that CTA is launched as four whole warpgroups (512 threads at 128 registers each) and
-// the registers are redistributed by warpgroup: the producer's warpgroup drops to
-// kProducerRegs and three of its warps leave, the two chain warpgroups rise to
-// kChainRegs, the prep warpgroup keeps 128. Per scheduler that is 2 x 168 + 128 + 24 =
-// 488 of its 512 registers per thread slot (62,464 of the CTA's 65,536), so the rise
-// never waits on registers that are not there.
+// warps of a dk = 128 state want about 157 and measure slower squeezed, so those CTAs are
+// launched as four whole warpgroups (512 threads at 128 registers each) and the registers
+// are redistributed by warpgroup: the producer's warpgroup drops to kProducerRegs and three
+// of its warps leave, the chain warpgroups rise to kChainRegs, the prep warpgroups keep 128.
+// Over 128 rows that is two chain warpgroups and one prep warpgroup (2 x 168 + 128 + 24 =
+// 488 of a scheduler's 512 registers per thread slot); over 64 rows, one chain warpgroup
+// and two prep warpgroups, a gram tile per prep warp (168 + 2 x 128 + 24 = 448). Either way
+// the rise never waits on registers that are not there.
 constexpr int kChainRegs = 168, kProducerRegs = 24;
 template <int DK, int DVC>
-constexpr bool prefill_regsplit() { return DK == 128 && DVC == 128; }
+constexpr bool prefill_regsplit() { return DK == 128; }
+// prep threads: two warpgroups for the 64-row CTA of a dk = 128 state (one gram tile per warp)
+template <int DK, int DVC>
+constexpr int prefill_prep_threads() { return (DK == 128 && DVC == 64) ? 2 * kPrepThreads : kPrepThreads; }
 template <int DK, int DVC, int RT>
 constexpr int prefill_threads() {
-    return DVC * 2 / RT + kPrepThreads + (prefill_regsplit<DK, DVC>() ? 4 * kProducerThreads : kProducerThreads);
+    return DVC * 2 / RT + prefill_prep_threads<DK, DVC>() +
+           (prefill_regsplit<DK, DVC>() ? 4 * kProducerThreads : kProducerThreads);
 }
 static_assert(2 * kChainRegs + 65536 / 512 + kProducerRegs <= 512, "register split exceeds a scheduler's file");
+static_assert(kChainRegs + 2 * (65536 / 512) + kProducerRegs <= 512, "register split exceeds a scheduler's file");
 
 template <int N>
 __device__ __forceinline__ void regs_raise() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -258,9 +264,10 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                   const __half *s_in, __half *s_out) {
     using L = PrefillSmem<DK, DVC>;
     constexpr int C = L::C, NSUB = L::NSUB, KH = L::KH, VH = L::VH;
-    constexpr int NW = DVC / (16 * RT), NTC = NW * 32, NTP = kPrepThreads, NTALL = NTC + NTP;
+    constexpr int NW = DVC / (16 * RT), NTC = NW * 32, NTP = prefill_prep_threads<DK, DVC>(), NTALL = NTC + NTP;
     constexpr bool SPLIT = prefill_regsplit<DK, DVC>();
-    static_assert(!SPLIT || (NW == 8 && kPrepThreads == 128), "the register split assumes 2 + 1 + 1 warpgroups");
+    static_assert(!SPLIT || ((NW == 8 && NTP == 128) || (NW == 4 && NTP == 256)),
+                  "the register split assumes 4 whole warpgroups of 128 registers");
     constexpr int NTX = kProducerThreads;  // the producer warp follows the prep warps
     constexpr int NTK = DK / 8;   // accumulator tiles of the state over dk
     constexpr int KS = DK / 16;   // k-steps of the projection

@@ -227,9 +227,9 @@ constexpr int kPrepThreads = 128, kProducerThreads = 32;
 constexpr int kChainRegs = 168, kProducerRegs = 24;
 template <int DK, int DVC>
 constexpr bool prefill_regsplit() { return DK == 128; }
-// prep threads: two warpgroups for the 64-row CTA of a dk = 128 state (one gram tile per warp)
+// prep threads: two warpgroups for 64-row CTAs (one gram tile per warp), one for 128 rows
 template <int DK, int DVC>
-constexpr int prefill_prep_threads() { return (DK == 128 && DVC == 64) ? 2 * kPrepThreads : kPrepThreads; }
+constexpr int prefill_prep_threads() { return DVC == 64 ? 2 * kPrepThreads : kPrepThreads; }
 template <int DK, int DVC, int RT>
 constexpr int prefill_threads() {
     return DVC * 2 / RT + prefill_prep_threads<DK, DVC>() +

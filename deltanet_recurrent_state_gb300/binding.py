@@ -192,6 +192,24 @@ def dn_accept_greedy(logits, draft_ids, target_ids=None, accepted_len=None, work
     return target_ids, accepted_len
 
 
+def dn_accept_greedy_noalloc(logits, draft_ids, target_ids, accepted_len, stream=None):
+    """dn_accept_greedy with its scratch in the library's fixed device array (no workspace).
+
+    For callers that cannot allocate device memory where they verify; the outputs must
+    be passed in. Calls that overlap on one GPU race on the shared array.
+    """
+    B, T, V = logits.shape
+    _dev(logits, draft_ids, target_ids, accepted_len)
+    assert draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32
+    assert target_ids.shape == (B, T) and target_ids.dtype == torch.int32
+    assert accepted_len.shape == (B,) and accepted_len.dtype == torch.int32
+    st = load_library().dn_accept_greedy_noalloc(
+        B, T, V, _DT[logits.dtype], _ptr(logits), _ptr(draft_ids), _ptr(target_ids),
+        _ptr(accepted_len), _stream(stream))
+    _check("dn_accept_greedy_noalloc", st)
+    return target_ids, accepted_len
+
+
 def dn_commit(ckpt, accepted_len, state, stream=None):
     """ckpt [N,T,H,dv,dk], accepted_len [B] int32 (device), state [N,H,dv,dk] updated in place."""
     N, H, dv, dk = state.shape

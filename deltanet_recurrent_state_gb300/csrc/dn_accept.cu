@@ -5,7 +5,8 @@
 // logits row, and the accepted length is the longest prefix on which the drafts
 // equal the targets.
 //
-// One pass over the logits. Grid = (chunks of kChunk vocab entries) x (B*T rows).
+// One pass over the logits. One CTA per (row, chunk of kChunk vocab entries), B*T rows,
+// numbered row-major on grid.x (so the row count is not bounded by grid.y).
 // Each CTA reduces its chunk to one 64-bit key, (order-preserving value bits << 32)
 // | (0xffffffff - index), so an unsigned max picks the largest value and, among
 // equal values, the lowest index; the order of the reduction cannot change the
@@ -18,6 +19,7 @@
 // finishes them, so the workspace is ready for the next call. Nothing spins or waits.
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -34,6 +36,13 @@ constexpr int kFlatRows = 16;  // up to this many rows (B x T), the one-level re
 __host__ __device__ inline int accept_chunks(int V) { return (V + kChunk - 1) / kChunk; }
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// One CTA per (row, chunk) on grid.x: at most 2^31 - 1 of them; the last row's index must
+// also fit the int32 target/draft arrays.
+inline bool accept_grid_ok(int B, int T, int V) {
+    const long long rows = (long long)B * T;
+    return rows <= 0x7fffffffLL && rows * accept_chunks(V) <= 0x7fffffffLL;
+}
 
 struct AcceptWorkspace {
     unsigned long long *keys;   // [rows][chunks]
@@ -59,7 +68,7 @@ __host__ __device__ inline AcceptWorkspace accept_ws(void *base, int B, int T, i
     return w;
 }
 
-// Order-preserving maps of the value bits to unsigned integers (finite inputs).
+// Order-preserving maps of the value bits to unsigned integers (any value but NaN).
 // -0.0 is folded onto +0.0 first, so the two compare equal as numbers do.
 __device__ __forceinline__ unsigned int order_key(unsigned short h) {
     if ((h & 0x7fffu) == 0) h = 0;
@@ -100,15 +109,14 @@ template <> struct Bits<unsigned int> { static constexpr int kVec = 4; };
 // FLAT: the one-level reduction (rows <= kFlatRows), chosen at launch.
 template <typename E, bool FLAT>
 __global__ void __launch_bounds__(kThreads)
-accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
+accept_greedy_kernel(int B, int T, int V, int chunks, const E *__restrict__ logits,
                      const int *__restrict__ draft, int *__restrict__ target,
                      int *__restrict__ accepted, AcceptWorkspace ws) {
     constexpr int VEC = Bits<E>::kVec;
     __shared__ unsigned long long red[kThreads / 32];
     __shared__ int is_last;
-    const int chunks = gridDim.x;
-    const int c = blockIdx.x;
-    const int row = blockIdx.y;
+    const int c = (int)(blockIdx.x % (unsigned)chunks);
+    const int row = (int)(blockIdx.x / (unsigned)chunks);
     const E *rp = logits + (size_t)row * V;
     const int c0 = c * kChunk;
     const int c1 = min(V, c0 + kChunk);
@@ -130,8 +138,9 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
         }
         if constexpr (VEC == 8) {
             // fp16: the thread's maximum by packed max, then the lowest index holding it (its
-            // elements are in increasing index order); -0 and +0 compare equal, as numbers do
-            const __half2 lowest = __halves2half2(__ushort_as_half(0xfbffu), __ushort_as_half(0xfbffu));
+            // elements are in increasing index order); -0 and +0 compare equal, as numbers do.
+            // The running maximum starts at -inf, so a row masked to -inf still finds index 0.
+            const __half2 lowest = __halves2half2(__ushort_as_half(0xfc00u), __ushort_as_half(0xfc00u));
             __half2 m2 = lowest;
 #pragma unroll
             for (int r = 0; r < kPer; ++r) {
@@ -174,7 +183,7 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
     best = block_max(best, red);
 
     if constexpr (FLAT) {
-        const int rows = gridDim.y;
+        const int rows = B * T;
         // One level: the last CTA of the grid reduces every row, then every request.
         __shared__ int s_tgt[kFlatRows];
         if (threadIdx.x == 0) {
@@ -260,9 +269,10 @@ accept_greedy_kernel(int B, int T, int V, const E *__restrict__ logits,
 template <typename E, bool FLAT>
 void launch_accept_as(int B, int T, int V, const void *logits, const int32_t *draft, int32_t *target,
                       int32_t *accepted, const AcceptWorkspace &ws, cudaStream_t st) {
-    const dim3 grid(accept_chunks(V), B * T);
-    accept_greedy_kernel<E, FLAT><<<grid, kThreads, 0, st>>>(B, T, V, static_cast<const E *>(logits), draft,
-                                                             target, accepted, ws);
+    const int chunks = accept_chunks(V);
+    const unsigned grid = (unsigned)((long long)B * T * chunks);
+    accept_greedy_kernel<E, FLAT><<<grid, kThreads, 0, st>>>(B, T, V, chunks, static_cast<const E *>(logits),
+                                                             draft, target, accepted, ws);
 }
 
 void launch_accept(int B, int T, int V, dn_dtype logit_dt, const void *logits, const int32_t *draft,
@@ -291,7 +301,7 @@ extern "C" dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, co
                                       size_t workspace_bytes, dn_stream_t stream) {
     using namespace dn;
     if (B < 0 || T < 1 || V < 1 || !dtype_ok(logit_dt)) return DN_ERR_INVALID_ARG;
-    if ((long long)B * T > 65535) return DN_ERR_INVALID_ARG;  // grid.y limit
+    if (!accept_grid_ok(B, T, V)) return DN_ERR_INVALID_ARG;
     if (B == 0) return DN_OK;
     if (!logits || !draft_ids || !target_ids || !accepted_len || !workspace) return DN_ERR_INVALID_ARG;
     if (!aligned(logits, 16) || !aligned(draft_ids, 4) || !aligned(target_ids, 4) ||
@@ -312,26 +322,68 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DN_ACCEPT_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch per device. In host code the array's name is
-// only a host-side stand-in; the kernel must be given the address the runtime reports.
-constexpr int kMaxDevices = 64;
+// Device address of g_noalloc_scratch. In host code the array's name is only a host-side
+// stand-in; the kernel must be given the address the runtime reports, and that address
+// belongs to one CUDA context: a device reset, or a second context on the same device,
+// loads the module again and may place the array elsewhere. So the address is looked up
+// once per context and cached under the context's unique id (cuCtxGetId, never reused
+// within a process), not under the device ordinal.
+typedef CUresult (*PFN_ctx_get_current)(CUcontext *);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long *);
+
+struct NoallocSlot {
+    unsigned long long ctx_id;
+    void *addr;
+};
+constexpr int kNoallocSlots = 64;
 std::mutex g_noalloc_mu;
-void *g_noalloc_addr[kMaxDevices] = {};
+NoallocSlot g_noalloc_slots[kNoallocSlots] = {};
+int g_noalloc_next = 0;
+
+template <typename F>
+F driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return reinterpret_cast<F>(p);
+}
+
+// Unique id of the calling thread's current context, or 0 when it has none yet.
+dn_status current_ctx_id(unsigned long long *id) {
+    static const PFN_ctx_get_current get_current = driver_fn<PFN_ctx_get_current>("cuCtxGetCurrent");
+    static const PFN_ctx_get_id get_id = driver_fn<PFN_ctx_get_id>("cuCtxGetId");
+    if (!get_current || !get_id) return DN_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return DN_ERR_CUDA;
+    *id = 0;
+    if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return DN_ERR_CUDA;
+    return DN_OK;
+}
 
 dn_status noalloc_scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return DN_ERR_CUDA;
+    unsigned long long id = 0;
+    if (current_ctx_id(&id) != DN_OK) return DN_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (dev >= 0 && dev < kMaxDevices && g_noalloc_addr[dev] != nullptr) {
-        *out = g_noalloc_addr[dev];
-        return DN_OK;
-    }
+    if (id != 0)
+        for (const NoallocSlot &sl : g_noalloc_slots)
+            if (sl.addr != nullptr && sl.ctx_id == id) {
+                *out = sl.addr;
+                return DN_OK;
+            }
+    // First call in this context (the lookup also creates the current device's primary
+    // context if the thread had none, so the id is read again after it).
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
         cudaGetLastError();
         return DN_ERR_CUDA;
     }
-    if (dev >= 0 && dev < kMaxDevices) g_noalloc_addr[dev] = p;
+    if (id == 0 && (current_ctx_id(&id) != DN_OK || id == 0)) return DN_ERR_CUDA;
+    g_noalloc_slots[g_noalloc_next] = NoallocSlot{id, p};
+    g_noalloc_next = (g_noalloc_next + 1) % kNoallocSlots;
     *out = p;
     return DN_OK;
 }
@@ -345,7 +397,7 @@ extern "C" dn_status dn_accept_greedy_noalloc(int B, int T, int V, dn_dtype logi
                                               dn_stream_t stream) {
     using namespace dn;
     if (B < 0 || T < 1 || V < 1 || !dtype_ok(logit_dt)) return DN_ERR_INVALID_ARG;
-    if ((long long)B * T > 65535) return DN_ERR_INVALID_ARG;
+    if (!accept_grid_ok(B, T, V)) return DN_ERR_INVALID_ARG;
     if (B == 0) return DN_OK;
     if (!logits || !draft_ids || !target_ids || !accepted_len) return DN_ERR_INVALID_ARG;
     if (!aligned(logits, 16) || !aligned(draft_ids, 4) || !aligned(target_ids, 4) ||

@@ -5,7 +5,8 @@
 // the DeltaNet state this is a copy of one checkpoint page (all heads of one
 // state set) over the state, or nothing when no draft was accepted.
 //
-// Pure copy, HBM bound: grid = (pieces of kPiece bytes per set) x N; each thread
+// Pure copy, HBM bound: one CTA per (set, piece of kPiece bytes), numbered set-major on
+// grid.x (so the set count is not bounded by grid.y); each thread
 // moves kUnroll 16-byte words with all loads issued before the stores. The
 // accepted length is read on the device, so no host round trip sits between
 // accept and commit.
@@ -24,15 +25,16 @@ constexpr int kUnroll = 8;
 constexpr size_t kPiece = (size_t)kThreads * kUnroll * 16;  // 32 KiB per CTA
 
 __global__ void __launch_bounds__(kThreads)
-commit_kernel(int B, int T, size_t set_bytes, const uint4 *__restrict__ ckpt,
+commit_kernel(int B, int T, unsigned pieces, size_t set_bytes, const uint4 *__restrict__ ckpt,
               const int *__restrict__ accepted, uint4 *__restrict__ state) {
-    const size_t n = blockIdx.y;
+    const size_t n = blockIdx.x / pieces;
+    const unsigned piece = blockIdx.x % pieces;
     const int a = __ldg(&accepted[n % B]);
     if (a < 1 || a > T) return;  // a == 0: keep the state; out of range: ignored
     const size_t words = set_bytes / 16;
     const uint4 *src = ckpt + (n * T + (a - 1)) * words;
     uint4 *dst = state + n * words;
-    const size_t base = blockIdx.x * (kPiece / 16) + threadIdx.x;
+    const size_t base = (size_t)piece * (kPiece / 16) + threadIdx.x;
     uint4 r[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -177,7 +179,7 @@ extern "C" dn_status dn_commit(int N, int B, int H, int T, int dk, int dv, dn_dt
     using namespace dn;
     if (N < 0 || B < 1 || H < 1 || T < 1 || T > DN_MAX_BLOCK || !dtype_ok(state_dt))
         return DN_ERR_INVALID_ARG;
-    if (N % B != 0 || N > 65535) return DN_ERR_INVALID_ARG;
+    if (N % B != 0) return DN_ERR_INVALID_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv)) return DN_ERR_UNSUPPORTED;
     if (N == 0) return DN_OK;
     if (!ckpt || !accepted_len || !state) return DN_ERR_INVALID_ARG;
@@ -185,10 +187,10 @@ extern "C" dn_status dn_commit(int N, int B, int H, int T, int dk, int dv, dn_dt
         return DN_ERR_INVALID_ARG;
     const size_t set_bytes = (size_t)H * dv * dk * dtype_bytes(state_dt);
     const size_t pieces = (set_bytes + kPiece - 1) / kPiece;
-    if (pieces > 0x7fffffffULL) return DN_ERR_INVALID_ARG;
-    const dim3 grid((unsigned)pieces, (unsigned)N);
+    if ((unsigned long long)pieces * (unsigned long long)N > 0x7fffffffULL) return DN_ERR_INVALID_ARG;
+    const unsigned grid = (unsigned)(pieces * (size_t)N);
     commit_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        B, T, set_bytes, static_cast<const uint4 *>(ckpt), accepted_len,
+        B, T, (unsigned)pieces, set_bytes, static_cast<const uint4 *>(ckpt), accepted_len,
         static_cast<uint4 *>(state));
     return launch_status();
 }

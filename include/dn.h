@@ -171,7 +171,9 @@ size_t dn_accept_workspace_bytes(int B, int T, int V);
  *   accepted_len[b]   = the first t with draft_ids[b][t] != target_ids[b][t], or T
  *
  *   logits        [B][T][V] logit_dt (DN_F16 or DN_F32), 16-byte aligned;
- *                 every value finite (not checked)
+ *                 any value but NaN (not checked): -inf marks a masked vocabulary
+ *                 entry, and a row that is -inf throughout gives target 0 in
+ *                 both dtypes
  *   draft_ids     [B][T] int32, 4-byte aligned
  *   target_ids    [B][T] int32, written
  *   accepted_len  [B] int32, written; stays on the device (dn_commit reads it
@@ -181,7 +183,8 @@ size_t dn_accept_workspace_bytes(int B, int T, int V);
  *                 after allocating it); every call leaves it ready for the
  *                 next one. Calls that may run concurrently need separate
  *                 workspaces.
- *   B >= 0, T >= 1, V >= 1, B * T <= 65535.
+ *   B >= 0, T >= 1, V >= 1; B * T * ceil(V / 8192) <= 2^31 - 1 (one CTA per
+ *   row and 8,192-entry chunk), else DN_ERR_INVALID_ARG.
  */
 dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, const void *logits,
                            const int32_t *draft_ids, int32_t *target_ids,
@@ -199,7 +202,8 @@ dn_status dn_accept_greedy(int B, int T, int V, dn_dtype logit_dt, const void *l
  *     1 <= a <= T   : state[n] = ckpt[n][a-1]     (all H heads)
  *     otherwise     : state[n] unchanged (an out-of-range length is ignored)
  *
- *   N multiple of B, N <= 65535; state set n belongs to request n % B (sets
+ *   N multiple of B, N * ceil(H * dv * dk * size / 32 KiB) <= 2^31 - 1 (one CTA
+ *   per 32 KiB piece of a set); state set n belongs to request n % B (sets
  *   laid out [layer][request], n = layer * B + request).
  *   ckpt          [N][T][H][dv][dk] state_dt, 16-byte aligned (dn_verify_block's)
  *   accepted_len  [B] int32 in device memory, 4-byte aligned
@@ -277,8 +281,12 @@ dn_status dn_prefill_checkpoint_tc(int N, int H, int P, int chunk, int dk, int d
  *     enqueued (about 1,600 verified positions at V = 151,936). Other arguments are
  *     checked as for dn_accept_greedy.
  *   - First call on a device: it looks up the array's device address once per
- *     device (with that device current) and returns DN_ERR_CUDA if the lookup
- *     fails. Make that first call before any stream capture on that device.
+ *     CUDA context (with that device current; in the runtime's usual use, one
+ *     primary context per device) and returns DN_ERR_CUDA if the lookup fails.
+ *     Make that first call before any stream capture on that device. The address
+ *     is cached under the context's unique id, so after cudaDeviceReset (which
+ *     destroys the context and unloads the array) or in a second context on the
+ *     same device the next call looks it up again instead of using a stale one.
  *   - Sharing: all calls on a device share the one array. The call clears the
  *     counters it needs on `stream` before its kernel runs, so leftovers of an
  *     earlier call do no harm; but two calls whose work overlaps on the GPU (on

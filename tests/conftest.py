@@ -19,3 +19,19 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.fail("a gpu-marked test ran without a CUDA device")
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    # both error measures of every GPU-vs-oracle check, worst case per check name
+    from tests import parity
+    if not parity.REPORT:
+        return
+    worst = {}
+    for name, e, ee, tol in parity.REPORT:
+        w = worst.setdefault(name, [0.0, 0.0, tol, 0])
+        w[0], w[1], w[3] = max(w[0], e), max(w[1], ee), w[3] + 1
+    terminalreporter.section("parity: per-tensor max|d|/max|ref| (asserted) and element-wise max |d|/(|ref|+1e-3)")
+    for name in sorted(worst):
+        e, ee, tol, n = worst[name]
+        terminalreporter.write_line("%-28s checks %4d  per-tensor %.3g (bar %.0e)  element-wise %.3g" % (
+            name, n, e, tol, ee))

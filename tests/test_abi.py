@@ -117,7 +117,7 @@ def _accept_args(buf, **over):
 
 @pytest.mark.parametrize("over", [
     dict(T=0), dict(V=0), dict(B=-1), dict(dt=5), dict(logits=None), dict(ws=None), dict(wsb=8),
-    dict(B=20000, T=4), "misaligned_logits", "misaligned_draft",
+    dict(B=300_000_000, T=8, V=151936), "misaligned_logits", "misaligned_draft",
 ])
 def test_accept_rejects(lib, over):
     buf = Bufs()
@@ -139,7 +139,7 @@ def _commit_args(buf, **over):
 @pytest.mark.parametrize("over,want", [
     (dict(B=0), INVALID), (dict(N=3, B=2), INVALID), (dict(T=17), INVALID),
     (dict(dk=100), UNSUPPORTED), (dict(s=None), INVALID), (dict(acc=None), INVALID),
-    ("misaligned_state", INVALID), (dict(N=70000, B=1), INVALID),
+    ("misaligned_state", INVALID), (dict(N=50_000_000, B=1, H=48, dk=128, dv=128), INVALID),
 ])
 def test_commit_rejects(lib, over, want):
     buf = Bufs()
@@ -220,3 +220,16 @@ def test_prefill_tc_rejects(lib, over, want):
         over = dict(out=buf(offset=4))
     base.update(over)
     assert lib.dn_prefill_checkpoint_tc(*_prefill_args(buf, **base)) == want
+
+
+def test_package_exports_every_binding_entry_point():
+    # every name the package advertises resolves, and every public binding function is advertised
+    import inspect
+    import deltanet_recurrent_state_gb300 as pkg
+    from deltanet_recurrent_state_gb300 import binding
+    for name in pkg._API:
+        assert getattr(pkg, name) is getattr(binding, name), name
+    public = {n for n, f in vars(binding).items()
+              if (inspect.isfunction(f) or inspect.isclass(f)) and not n.startswith("_")
+              and f.__module__ == binding.__name__}
+    assert public <= set(pkg._API), public - set(pkg._API)

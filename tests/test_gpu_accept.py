@@ -95,3 +95,29 @@ def test_workspace_reused_across_calls(B, T, cuda):
     assert int(ws.count_nonzero()) > 0  # keys stay, counters are zero again
     n_keys = B * T * ((V + 8191) // 8192) * 8
     assert int(ws[n_keys:].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.float32])
+def test_masked_rows_with_minus_infinity(dt, cuda):
+    # vocabulary entries masked to -inf: a row that is -inf throughout gives index 0 in both
+    # dtypes, a row with one finite entry gives that entry, and +inf wins like any maximum
+    V = 9000  # two chunks, the last one partly filled
+    logits = torch.full((2, 4, V), float("-inf"), dtype=dt)
+    logits[0, 1, 8500] = -3.0
+    logits[0, 2, 17] = float("inf")
+    logits[0, 2, 4000] = float("inf")
+    logits[0, 3, 8999] = -65504.0
+    logits[1] = (torch.randn((4, V), generator=torch.Generator().manual_seed(2)) * 2).to(dt)
+    logits[1, :, ::2] = float("-inf")
+    draft = torch.tensor([[0, 8500, 17, 8999], [0, 0, 0, 0]], dtype=torch.int32)
+    tgt, acc = _check(logits, draft, cuda)
+    assert list(tgt[0]) == [0, 8500, 17, 8999] and acc[0] == 4
+
+
+def test_more_rows_than_a_grid_y_dimension(cuda):
+    # 70,000 rows: the row count lives on grid.x, not on the 65,535-wide grid.y
+    B, T, V = 35000, 2, 40
+    gen = torch.Generator().manual_seed(11)
+    logits = torch.randint(-4, 5, (B, T, V), generator=gen).float()  # many ties
+    tgt_ref, _ = oracle.accept_greedy(logits.double().numpy(), np.zeros((B, T), np.int32))
+    _check(logits, _drafts_from(tgt_ref, V, gen), cuda)

@@ -71,3 +71,24 @@ def test_verify_accept_commit_chain_matches_oracle(dt, cuda):
                                    g["state"][n:n + 1].contiguous())
         torch.cuda.synchronize()
         assert torch.equal(cp[0, an - 1], state[n])
+
+
+def test_more_sets_than_a_grid_y_dimension(cuda):
+    # 70,000 state sets: the set count lives on grid.x, not on the 65,535-wide grid.y
+    N, B, H, T, d = 70000, 7, 1, 2, 64
+    gen = torch.Generator(device=cuda).manual_seed(4)
+    ckpt = torch.randn((N, T, H, d, d), generator=gen, device=cuda).half()
+    state = torch.randn((N, H, d, d), generator=gen, device=cuda).half()
+    a = torch.tensor([0, 1, 2, 1, 2, 0, 1], dtype=torch.int32)
+    before = state.clone()
+    dn.dn_commit(ckpt, a.to(cuda), state)
+    torch.cuda.synchronize()
+    pick = list(range(0, 9)) + list(range(65530, 65545)) + list(range(N - 9, N))
+    # the oracle maps set i of its batch to request i % B': give it one request per picked set
+    a_pick = np.array([int(a[n % B]) for n in pick], dtype=np.int32)
+    ref = oracle.commit(np64(before[pick]), np64(ckpt[pick]), a_pick)
+    np.testing.assert_array_equal(np64(state[pick]), ref)
+    # every set: changed exactly where its request accepted a token
+    changed = (state != before).flatten(1).any(1).cpu()
+    want = torch.tensor([int(a[n % B]) > 0 for n in range(N)])
+    assert torch.equal(changed, want)

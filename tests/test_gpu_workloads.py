@@ -70,6 +70,14 @@ def _verify_step_workload(name, cuda, sample):
         assert_close("committed state", state[n, h], want, TOL[w["state"]])
 
 
+def test_tiny_workload_end_to_end(cuda):
+    # 1 layer, 1 request, 4 heads, dk = dv = 64, T = 8, fp32 state, V = 512 fp32 logits,
+    # a ~ U{0..T}: verify -> accept -> commit, every unit against the oracle (the sample is
+    # all N * H = 4 units), ids and the accepted length bit-exact
+    w = WORKLOADS["tiny_h4_d64_t8_f32"]
+    _verify_step_workload("tiny_h4_d64_t8_f32", cuda, sample=w["L"] * w["B"] * w["H"])
+
+
 def test_single_user_t16_full_size(cuda):
     _verify_step_workload("single_user_l48_h48_d128_t16_f16", cuda, sample=12)
 

@@ -245,3 +245,47 @@ def test_context_drafts_mutant_is_caught(kind, monkeypatch):
     monkeypatch.setattr(oracle, "context_drafts_row", _context_mutant(kind))
     with pytest.raises(AssertionError):
         pins.test_context_drafts_handworked_golden()
+
+
+def _round_mutant(kind):
+    real = rec.round_to
+
+    def round_to(x, dtype):
+        x = np.asarray(x, dtype=np.float64)
+        if dtype != "f16":
+            return real(x, dtype)
+        with np.errstate(over="ignore"):
+            if kind == "double_rounding":
+                # wrong: rounds to binary32 first, then to binary16
+                return x.astype(np.float32).astype(np.float16).astype(np.float64)
+            near = x.astype(np.float16).astype(np.float64)
+        if kind == "truncate":
+            # wrong: rounds toward zero (drops the bits below the last fraction bit)
+            over = np.abs(near) > np.abs(x)
+            toward0 = np.nextafter(near.astype(np.float16), np.float16(0)).astype(np.float64)
+            return np.where(over, toward0, near)
+        if kind == "ties_away":
+            # wrong: exact ties go away from zero instead of to the even neighbour
+            up = np.nextafter(near.astype(np.float16), np.copysign(np.float16(np.inf), x).astype(np.float16))
+            up = up.astype(np.float64)
+            tie = np.abs(near - x) == np.abs(up - x)
+            return np.where(tie & (np.abs(up) > np.abs(near)), up, near)
+        raise ValueError(kind)
+    return round_to
+
+
+@pytest.mark.parametrize("kind", ["truncate", "double_rounding", "ties_away"])
+def test_round_to_mutant_is_caught(kind, monkeypatch):
+    mutant = _round_mutant(kind)
+    monkeypatch.setattr(rec, "round_to", mutant)
+    monkeypatch.setattr(oracle, "round_to", mutant)
+    with pytest.raises(AssertionError):
+        pins.test_round_to_handworked_round_to_nearest_even()
+    if kind != "ties_away":  # the store-path pin holds no exact tie
+        with pytest.raises(AssertionError):
+            pins.test_verify_and_prefill_stores_round_to_nearest_even()
+
+
+def test_unmutated_round_to_passes_its_pins():
+    assert _count_failures([pins.test_round_to_handworked_round_to_nearest_even,
+                            pins.test_verify_and_prefill_stores_round_to_nearest_even]) == 0

@@ -12,6 +12,8 @@ Speculation" (Technical Insight).
 """
 
 import os
+import re
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -86,6 +88,107 @@ def test_handworked_golden(case, store):
     for t, tok in enumerate(toks):
         assert np.array_equal(ckpt[0, t, 0], np.array(tok["S"]).reshape(dv, dk)), (case, t)
         assert np.array_equal(o[0, t, 0], np.array(tok["o"])), (case, t)
+
+
+# ----------------------------------------------------------------------------- store rounding
+
+def _exact(expr):
+    """An exact value written as a signed sum of terms c, c*2^e or 2^e (inf, -inf, -0 allowed).
+
+    Returns a float64. Every term is parsed as an exact rational (a decimal literal
+    stands for its nearest float64), so the sum is exact before the one final
+    conversion, and every input of the golden file is a float64 value.
+    """
+    if expr in ("inf", "-inf"):
+        return float(expr)
+    if expr == "-0":
+        return -0.0
+    total = Fraction(0)
+    for sign, term in re.findall(r"([+-]?)([^+-]+(?:\^-?\d+)?)", expr.replace("^-", "^~")):
+        term = term.replace("^~", "^-")
+        value = Fraction(1)
+        for factor in term.split("*"):
+            if factor.startswith("2^"):
+                value *= Fraction(2) ** int(factor[2:])
+            else:
+                value *= Fraction(float(factor)) if "." in factor else Fraction(int(factor))
+        total += -value if sign == "-" else value
+    x = float(total)
+    assert Fraction(x) == total, expr  # every value in the file is a float64
+    return x
+
+
+def _decode(fmt, bits):
+    """The value of an IEEE 754 binary16 / binary32 encoding, from the format's definition."""
+    ebits, fbits = {"f16": (5, 10), "f32": (8, 23)}[fmt]
+    bias = (1 << (ebits - 1)) - 1
+    s = bits >> (ebits + fbits)
+    e = (bits >> fbits) & ((1 << ebits) - 1)
+    f = bits & ((1 << fbits) - 1)
+    if e == (1 << ebits) - 1:
+        assert f == 0, "no NaN in the golden file"
+        mag = float("inf")
+    elif e == 0:
+        mag = float(Fraction(f, 1 << fbits) * Fraction(2) ** (1 - bias))
+    else:
+        mag = float((1 + Fraction(f, 1 << fbits)) * Fraction(2) ** (e - bias))
+    return -mag if s else mag
+
+
+def _parse_rounding_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "handworked_rounding.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            fmt, x, want, bits = line.split()
+            rows.append((fmt, x, want, int(bits, 16)))
+    return rows
+
+
+def _same_value(a, b):
+    return (a == b and np.signbit(a) == np.signbit(b)) or (np.isinf(a) and a == b)
+
+
+def test_rounding_golden_file_is_self_consistent():
+    # each expected value is the value its stated encoding decodes to
+    rows = _parse_rounding_golden()
+    assert sum(r[0] == "f16" for r in rows) >= 20 and sum(r[0] == "f32" for r in rows) >= 8
+    for fmt, _, want, bits in rows:
+        assert _same_value(_decode(fmt, bits), _exact(want)), (fmt, want, hex(bits))
+
+
+def test_round_to_handworked_round_to_nearest_even():
+    # oracle.round_to against hand-worked binary16 / binary32 roundings: ties to even,
+    # either side of a tie, carries into the next binade, subnormals, overflow, -0
+    for fmt, x, want, bits in _parse_rounding_golden():
+        with np.errstate(over="ignore"):
+            got = float(oracle.round_to(np.array([_exact(x)]), fmt)[0])
+        assert _same_value(got, _decode(fmt, bits)), (fmt, x, got, want)
+
+
+def test_verify_and_prefill_stores_round_to_nearest_even():
+    # the stores of verify_block and prefill_checkpoint carry the same rounding: with
+    # beta = 0 and g = 1 the state is unchanged and o = S q, so a hand-picked S and q
+    # put an exact value on each store. S0 = 1 + 2^-11 + 2^-30 (stored: 1 + 2^-10,
+    # not 1 as truncation or double rounding through binary32 would give); q = 1 + 2^-10,
+    # so o = S q = 1 + 3*2^-11 + 2^-21 + 2^-30 + 2^-40, just above the tie between
+    # 1 + 2^-10 and 1 + 2^-9: stored 1 + 2^-9 (truncation gives 1 + 2^-10).
+    s0 = _exact("1+2^-11+2^-30")
+    qv = _exact("1+2^-10")
+    o_exact = Fraction(s0) * Fraction(qv)
+    assert Fraction(_exact("1+3*2^-11")) < o_exact < Fraction(_exact("1+2^-9"))
+    one = np.ones((1, 1, 1, 1))
+    args = dict(q=qv * one, k=one, v=one, beta=np.zeros((1, 1, 1)), g=np.ones((1, 1, 1)))
+    o, ck = oracle.verify_block(args["q"], args["k"], args["v"], args["beta"], args["g"],
+                                s0 * np.ones((1, 1, 1, 1)), store="f16", io="f16")
+    assert ck[0, 0, 0, 0, 0] == _exact("1+2^-10")
+    assert o[0, 0, 0, 0] == _exact("1+2^-9")
+    o2, ck2, sf = oracle.prefill_checkpoint(args["q"], args["k"], args["v"], args["beta"], args["g"],
+                                            s0 * np.ones((1, 1, 1, 1)), chunk=1, store="f16", io="f16")
+    assert ck2[0, 0, 0, 0, 0] == _exact("1+2^-10") and sf[0, 0, 0, 0] == _exact("1+2^-10")
+    assert o2[0, 0, 0, 0] == _exact("1+2^-9")
 
 
 # ----------------------------------------------------------------------------- closed forms

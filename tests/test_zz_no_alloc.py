@@ -6,16 +6,17 @@ or C code embedded in a host whose allocator it cannot reach. It keeps its scrat
 in a fixed array inside libdn.so instead of a caller workspace. These tests call
 it through the C ABI and require the same target ids and accepted lengths
 (bit-exact, as for every integer result here) as dn_accept_greedy on the same
-inputs, on two calls in a row, plus the size limit. They depend on no other test,
-so they pass alone in a fresh process and after the rest of the suite.
+inputs, on two calls in a row, plus the size limit; and the same results as the
+float64 oracle directly, also right after a larger call has left its scratch
+full of non-zero keys where the next call keeps its counters. They depend on no
+other test, so they pass alone in a fresh process and after the rest of the suite.
 """
-
-import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from deltanet_recurrent_state_gb300 import binding as dn
 from deltanet_recurrent_state_gb300 import inputs
 
@@ -81,3 +82,25 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda):
     torch.cuda.synchronize()
     assert st == dn.DN_ERR_INVALID_ARG
     assert (tgt == -7).all() and (acc == -7).all()
+
+
+def test_noalloc_matches_oracle_after_a_larger_call_left_leftovers(cuda):
+    # A call over many rows fills the front of the shared array with its chunk keys (never
+    # zero: every key carries the value's order bits). The next, smaller call keeps its
+    # counters at an offset inside that region, so it is right only if it clears them first.
+    lib = dn.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    V = 151936
+    chunks = (V + 8191) // 8192
+    big_rows, small = 1500, (1, 16)
+    assert dn.dn_accept_workspace_bytes(big_rows, 1, V) <= SCRATCH_LIMIT
+    small_counter_offset = small[0] * small[1] * chunks * 8  # keys first, 16-byte aligned
+    assert small_counter_offset % 16 == 0 and small_counter_offset < big_rows * chunks * 8
+    for B, T in ((big_rows, 1), small, (big_rows, 1), (3, 5)):
+        logits, draft = _case(B, T, V, "f16", 920 + B + T, cuda)
+        st, tgt, acc = _noalloc(lib, logits, draft, stream)
+        assert st == dn.DN_OK, dn.dn_status_string(st)
+        torch.cuda.synchronize()
+        tgt_ref, acc_ref = oracle.accept_greedy(logits.double().cpu().numpy(), draft.cpu().numpy())
+        np.testing.assert_array_equal(tgt.cpu().numpy(), tgt_ref)
+        np.testing.assert_array_equal(acc.cpu().numpy(), acc_ref)

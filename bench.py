@@ -553,6 +553,63 @@ def deltas_row(sets, device, stream, steps=200, warmup=5):
             "algorithmic_bytes_per_step": vb + cb + accept_bytes(B, T, w["V"], 2)}
 
 
+def verify_per_layer_row(sets, device, stream, reps=50, warmup=5):
+    """The single-user verify as a model runs it, one layer at a time: 48 launches of
+    dn_verify_block over one state set each (B = 1, 48 heads, T = 16; layer l + 1's q/k/v
+    come out of layer l), captured in one CUDA graph per buffer set and timed per replay,
+    beside the same 48 layers folded into one launch."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS[HEADLINE]
+    L, T, H, dk, dv = w["L"], w["T"], w["H"], w["dk"], w["dv"]
+
+    def layers(x):
+        for l in range(L):
+            sl = {k: x[k][l:l + 1] for k in ("q", "k", "v", "beta", "g", "state", "out", "ckpt")}
+            dn.dn_verify_block(sl["q"], sl["k"], sl["v"], sl["beta"], sl["g"], sl["state"], sl["out"],
+                               sl["ckpt"], stream=stream)
+
+    def folded(x):
+        dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"], x["ckpt"],
+                           stream=stream)
+
+    res = {"workload": HEADLINE + " verify, one launch per layer", "layers": L}
+    for name, body in (("per_layer", layers), ("folded", folded)):
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                body(sets[i % len(sets)])
+        torch.cuda.synchronize()
+        gs = []
+        for x in sets:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                body(x)
+            gs.append(gr)
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                gs[i % len(gs)].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for i in range(reps):
+                gs[i % len(gs)].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        vb = verify_bytes(L, T, H, dk, dv, 2)
+        res[name] = {"ms_per_48_layers": ms, "us_per_layer": ms / L * 1e3,
+                     "gbs": vb / (ms / 1e3) / 1e9, "token_layers_per_s": T * L / (ms / 1e3)}
+        del gs
+    hbm, _ = peaks()
+    for name in ("per_layer", "folded"):
+        res[name]["frac"] = res[name]["gbs"] / hbm
+    res["bytes_per_layer_launch"] = verify_bytes(1, T, H, dk, dv, 2)
+    res["ctas_per_layer_launch"] = H * dv // 32
+    return res
+
+
 def decode_row(device, stream, steps=1000, warmup=10, nsets=8):
     """The single-user decode loop: 1000 consecutive verify (T = 8) -> accept -> commit steps
     timed as one loop, each step committing into the state the next step of its buffer set
@@ -781,6 +838,7 @@ def main():
 
     rows = {}
     if not args.no_rows and rank == 0:
+        rows["verify_per_layer"] = verify_per_layer_row(sets, device, stream)
         rows["recompute_on_commit_step"] = deltas_row(sets, device, stream)
         rows["decode_loop"] = decode_row(device, stream)
         rows["batch64_step"] = batch_row(device, stream)

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "dn.h"
+#include "dn_device.cuh"
 #include "dn_internal.h"
 
 namespace dn {
@@ -117,6 +118,8 @@ accept_greedy_kernel(int B, int T, int V, int chunks, const E *__restrict__ logi
     __shared__ int is_last;
     const int c = (int)(blockIdx.x % (unsigned)chunks);
     const int row = (int)(blockIdx.x / (unsigned)chunks);
+    grid_dep_wait();
+    grid_dep_trigger();
     const E *rp = logits + (size_t)row * V;
     const int c0 = c * kChunk;
     const int c1 = min(V, c0 + kChunk);
@@ -271,8 +274,8 @@ void launch_accept_as(int B, int T, int V, const void *logits, const int32_t *dr
                       int32_t *accepted, const AcceptWorkspace &ws, cudaStream_t st) {
     const int chunks = accept_chunks(V);
     const unsigned grid = (unsigned)((long long)B * T * chunks);
-    accept_greedy_kernel<E, FLAT><<<grid, kThreads, 0, st>>>(B, T, V, chunks, static_cast<const E *>(logits),
-                                                             draft, target, accepted, ws);
+    launch_pdl(accept_greedy_kernel<E, FLAT>, dim3(grid), dim3(kThreads), 0, st, B, T, V, chunks,
+               static_cast<const E *>(logits), draft, target, accepted, ws);
 }
 
 void launch_accept(int B, int T, int V, dn_dtype logit_dt, const void *logits, const int32_t *draft,

@@ -29,6 +29,8 @@ commit_kernel(int B, int T, unsigned pieces, size_t set_bytes, const uint4 *__re
               const int *__restrict__ accepted, uint4 *__restrict__ state) {
     const size_t n = blockIdx.x / pieces;
     const unsigned piece = blockIdx.x % pieces;
+    grid_dep_wait();
+    grid_dep_trigger();
     const int a = __ldg(&accepted[n % B]);
     if (a < 1 || a > T) return;  // a == 0: keep the state; out of range: ignored
     const size_t words = set_bytes / 16;
@@ -77,6 +79,8 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
     const int rb = blockIdx.x % rblocks;
     const int h = (blockIdx.x / rblocks) % H;
     const size_t n = blockIdx.x / (rblocks * H);
+    grid_dep_wait();
+    grid_dep_trigger();
     const int a = __ldg(&accepted[n % B]);
     if (a < 1 || a > T) return;  // a == 0: keep the state; out of range: ignored
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -167,9 +171,9 @@ extern "C" dn_status dn_commit_deltas(int N, int B, int H, int T, int dk, int dv
     const __half *kh = static_cast<const __half *>(k);
     __half *sh = static_cast<__half *>(state);
     if (dk == 128)
-        commit_deltas_kernel<128><<<blocks, 256, 0, st>>>(B, H, T, dv, kh, g, delta, accepted_len, sh);
+        launch_pdl(commit_deltas_kernel<128>, dim3(blocks), dim3(256), 0, st, B, H, T, dv, kh, g, delta, accepted_len, sh);
     else
-        commit_deltas_kernel<64><<<blocks, 256, 0, st>>>(B, H, T, dv, kh, g, delta, accepted_len, sh);
+        launch_pdl(commit_deltas_kernel<64>, dim3(blocks), dim3(256), 0, st, B, H, T, dv, kh, g, delta, accepted_len, sh);
     return launch_status();
 }
 
@@ -189,8 +193,8 @@ extern "C" dn_status dn_commit(int N, int B, int H, int T, int dk, int dv, dn_dt
     const size_t pieces = (set_bytes + kPiece - 1) / kPiece;
     if ((unsigned long long)pieces * (unsigned long long)N > 0x7fffffffULL) return DN_ERR_INVALID_ARG;
     const unsigned grid = (unsigned)(pieces * (size_t)N);
-    commit_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        B, T, (unsigned)pieces, set_bytes, static_cast<const uint4 *>(ckpt), accepted_len,
-        static_cast<uint4 *>(state));
+    launch_pdl(commit_kernel, dim3(grid), dim3(kThreads), 0, reinterpret_cast<cudaStream_t>(stream), B, T,
+               (unsigned)pieces, set_bytes, static_cast<const uint4 *>(ckpt), accepted_len,
+               static_cast<uint4 *>(state));
     return launch_status();
 }

@@ -8,6 +8,18 @@
 
 namespace dn {
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// The step kernels are launched with programmatic stream serialisation allowed (see
+// launch_pdl in dn_internal.h): a kernel may be scheduled while the kernel before it on
+// the stream is still running. Each calls grid_dep_wait() before its first global
+// memory access, which returns once every earlier kernel on the stream has completed and
+// its writes are visible, so results are as with plain stream order. Right after that
+// wait it calls grid_dep_trigger(), which lets the next kernel be scheduled onto free
+// SM slots meanwhile: its launch latency then overlaps this kernel's run. Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- 8 consecutive elements <-> 8 floats ---------------------------------------------
 
 __device__ __forceinline__ void load8(const __half *p, float (&x)[8]) {

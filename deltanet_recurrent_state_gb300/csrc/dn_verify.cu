@@ -54,6 +54,8 @@ verify_block_kernel(int H, int T, int DV, const IO *__restrict__ q, const IO *__
     const int lr = tid / TPR;
     const int ln = tid % TPR;
     const int row = rb * ROWS + lr;
+    grid_dep_wait();
+    grid_dep_trigger();
 
     // State slice -> registers (issued first so it overlaps the staging loads).
     float s[EPT];
@@ -161,7 +163,7 @@ __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
 // k/q tiles, the grams, L and M, the gate scan -- is shared by twice the rows).
 static_assert(DN_MAX_BLOCK == 16, "tile capacities 8 and 16");
 template <int DK, bool CKPT, int TM, int ROWS>
-__global__ void __launch_bounds__(256, ROWS == 64 ? 4 : (TM == 8 ? 6 : 5))
+__global__ void __launch_bounds__(256, ROWS == 64 ? 4 : (ROWS == 16 ? 6 : (TM == 8 ? 6 : 5)))
 verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
                  const __half *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ g, const __half *__restrict__ s_in,
@@ -185,6 +187,9 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     const int tid = threadIdx.x, lr = tid / TPR, ln = tid % TPR, row = rb * ROWS + lr;
     const int warp = tid / 32, lane = tid % 32;
     const size_t set_elems = (size_t)DV * DK;
+    static_assert(NCH >= 1, "a lane holds at least one 16-byte chunk of its row");
+    grid_dep_wait();
+    grid_dep_trigger();
 
     // 1. state chunks c*TPR + ln of this lane's row: fp16 to shared, fp32 to registers
     float2 s[NCH * 4];
@@ -291,7 +296,7 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     __syncthreads();
 
     // 4. delta_t by forward substitution, one lane per row
-    if (warp < ROWS / 32) {
+    if (warp * 32 + lane < ROWS) {
         const int rl = warp * 32 + lane;  // the row of this lane
         float dl[TM];
 #pragma unroll
@@ -351,17 +356,41 @@ constexpr int kTpr = 8;
 
 // State rows per CTA of verify_wy_kernel. With checkpoints, 32: the rows' state lives in
 // registers for the update, and 64-row CTAs measured slower (fewer CTAs per SM, spills at
-// T = 16). Writing deltas, 64: no state in registers, and the head's state-independent work
-// is shared by twice the rows (a whole head per CTA measured slower again).
-constexpr int kWyRowsCkpt = 32, kWyRowsDelta = 64;
+// T = 16). A launch of a few state sets (one layer of one request: 48 heads, 192 CTAs of 32
+// rows on 152 SMs) leaves some SMs with two CTAs' stores and others with one, so such
+// launches take 16-row CTAs (dk = 128, 16 lanes per row): twice the CTAs, an even spread,
+// each repeating its head's small state-independent work. Writing deltas, 64: no state in
+// registers, and the head's state-independent work is shared by twice the rows (a whole head
+// per CTA measured slower again).
+constexpr int kWyRowsCkpt = 32, kWyRowsCkptSmall = 16, kWyRowsDelta = 64;
+
+template <int DK, bool CKPT, int TM, int R>
+void launch_verify_wy_rows(int N, int H, int T, int dv, const __half *q, const __half *k, const __half *v,
+                           const float *beta, const float *g, const __half *s_in, __half *out, __half *ckpt,
+                           float *delta, cudaStream_t st) {
+    const unsigned blocks = (unsigned)((long long)N * H * (dv / R));
+    launch_pdl(verify_wy_kernel<DK, CKPT, TM, R>, dim3(blocks), dim3(256), 0, st, H, T, dv, q, k, v, beta, g,
+               s_in, out, ckpt, delta);
+}
 
 template <int DK, bool CKPT, int TM>
 void launch_verify_wy(int N, int H, int T, int dv, const __half *q, const __half *k, const __half *v,
                       const float *beta, const float *g, const __half *s_in, __half *out, __half *ckpt,
                       float *delta, cudaStream_t st) {
-    constexpr int R = CKPT ? kWyRowsCkpt : kWyRowsDelta;  // dv (64 or 128) is a multiple of both
-    const unsigned blocks = (unsigned)((long long)N * H * (dv / R));
-    verify_wy_kernel<DK, CKPT, TM, R><<<blocks, 256, 0, st>>>(H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta);
+    if constexpr (!CKPT) {
+        launch_verify_wy_rows<DK, CKPT, TM, kWyRowsDelta>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta, st);
+    } else if constexpr (DK == 128) {
+        // fewer 32-row CTAs than two per SM: the 16-row CTAs spread the stores evenly
+        const long long ctas32 = (long long)N * H * (dv / kWyRowsCkpt);
+        if (ctas32 < 2LL * device_sm_count())
+            launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkptSmall>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt,
+                                                                  delta, st);
+        else
+            launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkpt>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta,
+                                                             st);
+    } else {
+        launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkpt>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta, st);
+    }
 }
 
 template <int DK, typename IO, typename ST>
@@ -369,10 +398,9 @@ void launch_verify(int N, int H, int T, int dv, const void *q, const void *k, co
                    const float *beta, const float *g, const void *s_in, void *out, void *ckpt,
                    cudaStream_t st) {
     const long long blocks = (long long)N * H * (dv / kRows);
-    verify_block_kernel<DK, kRows, kTpr, IO, ST><<<(unsigned)blocks, kRows * kTpr, 0, st>>>(
-        H, T, dv, static_cast<const IO *>(q), static_cast<const IO *>(k),
-        static_cast<const IO *>(v), beta, g, static_cast<const ST *>(s_in),
-        static_cast<IO *>(out), static_cast<ST *>(ckpt));
+    launch_pdl(verify_block_kernel<DK, kRows, kTpr, IO, ST>, dim3((unsigned)blocks), dim3(kRows * kTpr), 0, st, H,
+               T, dv, static_cast<const IO *>(q), static_cast<const IO *>(k), static_cast<const IO *>(v), beta, g,
+               static_cast<const ST *>(s_in), static_cast<IO *>(out), static_cast<ST *>(ckpt));
 }
 
 }  // namespace

@@ -86,3 +86,25 @@ def test_outputs_do_not_spill_past_their_buffers(cuda):
     dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], out, ckpt)
     torch.cuda.synchronize()
     assert (out_buf[-64:] == 7.0).all() and (ck_buf[-64:] == 7.0).all()
+
+
+@pytest.mark.parametrize("T", [4, 16])
+def test_one_layer_launch_matches_folded_launch_and_oracle(T, cuda):
+    # One layer of one request (48 heads) is a small grid, which the library runs with
+    # 16-row CTAs; 48 layers folded into one launch run with 32-row CTAs. Both follow the
+    # same arithmetic per state row, so each layer's results are bit-identical, and a
+    # sample of heads matches the oracle.
+    L, H, d = 6, 48, 128
+    x = inputs.recurrence_inputs(L, T, H, d, d, seed=40 + T, device=cuda)
+    out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    for l in range(L):
+        sl = {k: x[k][l:l + 1] for k in ("q", "k", "v", "beta", "g", "state")}
+        o1, c1 = dn.dn_verify_block(sl["q"], sl["k"], sl["v"], sl["beta"], sl["g"], sl["state"])
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], out[l]) and torch.equal(c1[0], ckpt[l]), l
+    heads = [0, 17, 47]
+    u = {k: np64(x[k][0:1, :, heads]) for k in ("q", "k", "v", "beta", "g")}
+    o_ref, c_ref = oracle.verify_block(u["q"], u["k"], u["v"], u["beta"], u["g"],
+                                       np64(x["state"][0:1, heads]), store="f16", io="f16")
+    assert_close("out", out[0:1, :, heads], o_ref, TOL["f16"])
+    assert_close("ckpt", ckpt[0:1, :, heads], c_ref, TOL["f16"])

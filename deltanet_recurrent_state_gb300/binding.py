@@ -258,12 +258,12 @@ def dn_prefill_wait_timeouts():
     return int(load_library().dn_prefill_wait_timeouts())
 
 
-def dn_wait_selftest(tries, device=None, stream=None):
-    """Runs the bounded-wait self-test; returns (gave_up_unfinished, returned_finished)."""
-    result = torch.full((2,), -1, dtype=torch.int32, device=device or "cuda")
-    _check("dn_wait_selftest", load_library().dn_wait_selftest(int(tries), result.data_ptr(), _stream(stream)))
+def dn_wait_selftest(budget_us, device=None, stream=None):
+    """Runs the bounded-wait self-test; returns (gave_up, returned, drained, failures_counted)."""
+    result = torch.tensor([11, 22, 33, 44], dtype=torch.int32, device=device or "cuda")
+    _check("dn_wait_selftest", load_library().dn_wait_selftest(int(budget_us), result.data_ptr(), _stream(stream)))
     torch.cuda.synchronize(result.device)
-    return int(result[0]), int(result[1])
+    return tuple(int(x) for x in result.cpu())
 
 
 def dn_context_drafts(context, lengths, n_max=4, n_min=1, K=8, drafts=None, count=None,

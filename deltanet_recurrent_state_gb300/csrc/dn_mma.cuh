@@ -88,6 +88,64 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *mb, unsigned parit
     }
     return false;
 }
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A wait of the prefill kernels gives up after this long (the global timer, in ns): 1 s,
+// against waits of a few microseconds when the copies and MMAs they wait for progress.
+constexpr unsigned long long kWaitBudgetNs = 1000000000ull;
+
+// Bounded wait for the phase with the given parity by time: false if it did not complete
+// within `budget_ns`, or once `*abort` is set by another thread of the CTA (checked every
+// 64 polls). On its own timeout the wait raises `*abort` and counts the CTA's failure in
+// `*timeouts` once, so every role of the CTA stops issuing work at its next check.
+__device__ __forceinline__ bool mbar_wait_guarded(unsigned long long *mb, unsigned parity, volatile int *abort,
+                                                  unsigned int *timeouts,
+                                                  unsigned long long budget_ns = kWaitBudgetNs) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
+    const unsigned long long t0 = global_timer_ns();
+    for (int it = 0;; ++it) {
+        unsigned ok;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+        if ((it & 63) == 63) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > budget_ns) {
+                if (atomicExch(const_cast<int *>(abort), 1) == 0 && timeouts) atomicAdd(timeouts, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+// Drain of a copy this thread issued: waits at most `budget_ns` for the phase, ignoring any
+// abort (the copy was issued and lands unless something is broken); true if it landed.
+__device__ __forceinline__ bool mbar_drain(unsigned long long *mb, unsigned parity,
+                                           unsigned long long budget_ns = kWaitBudgetNs) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        unsigned ok;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+        if (global_timer_ns() - t0 > budget_ns) return false;
+    }
+}
+
+// Contiguous global -> shared copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned), completing on the mbarrier.
+__device__ __forceinline__ void bulk_load(void *smem, const void *gmem, unsigned bytes, unsigned long long *mb) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem);
+    const unsigned m = (unsigned)__cvta_generic_to_shared(mb);
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(d), "l"(gmem), "r"(bytes), "r"(m) : "memory");
+}
+
 // Box of a 4-d tensor map -> shared memory, completing `bytes` on the mbarrier.
 __device__ __forceinline__ void tma_load_4d(void *smem, const void *tmap, int c0, int c1, int c2, int c3,
                                             unsigned long long *mb) {

@@ -185,7 +185,8 @@ struct PrefillSmem {
     static constexpr size_t kA = kDec + NPREP * C * 4;                   // [NSUB][16][17] float
     static constexpr size_t kGates = kA + NSUB * 16 * 17 * 4;            // [3][2][C] float: beta, g
     static constexpr size_t kMbar = kGates + (size_t)NKQV * 2 * C * 4;   // [3] mbarrier
-    static constexpr size_t kBytes = kMbar + NKQV * 8;
+    static constexpr size_t kAbort = kMbar + NKQV * 8;                   // int: a wait ran out
+    static constexpr size_t kBytes = kAbort + 8;
 };
 
 // 16-byte chunk `ch` (of D/8) of row `r` in a run of 64-column swizzled boxes with
@@ -242,7 +243,6 @@ template <int N>
 __device__ __forceinline__ void regs_raise() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 template <int N>
 __device__ __forceinline__ void regs_lower() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-constexpr int kWaitTries = 1 << 22;  // polls before an input wait is reported as run out
 // 16-row state tiles per chain warp. Two tiles per warp halve the operand fragments each
 // warp loads from shared memory (which runs at about 80 % of its throughput here), but they
 // leave one chain warp per scheduler instead of two and need 128 fp32 state registers a
@@ -285,6 +285,10 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     float(*sA)[16][17] = reinterpret_cast<float(*)[16][17]>(smem + L::kA);
     float(*sGates)[2][C] = reinterpret_cast<float(*)[2][C]>(smem + L::kGates);  // [buf][beta|g][t]
     unsigned long long *mbar = reinterpret_cast<unsigned long long *>(smem + L::kMbar);
+    // Raised when a wait runs out (kWaitBudgetNs): from then on no role issues copies or global
+    // stores, every role still passes its named barriers to the end of the loop, and the
+    // producer waits (bounded) for the copies it issued before the CTA exits.
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L::kAbort);
 
     constexpr int RB = DV / DVC;  // CTAs per (sequence, head)
     const int rb = blockIdx.x % RB;
@@ -300,6 +304,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
 
     if (tid == NTC) {
         for (int b = 0; b < 3; ++b) mbar_init(&mbar[b], 1);
+        *abort = 0;
         fence_proxy_async();
     }
     __syncthreads();
@@ -332,22 +337,34 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
             regs_lower<kProducerRegs>();  // the whole warpgroup, then its spare warps leave
             if (warp != NW + NTP / 32) return;
         }
+        int last = -1;  // the last chunk whose copies were issued (lane 0); chunks load in order
         if (lane == 0)
-            for (int c = 0; c < min(3, nchunks); ++c) load_chunk(c);
+            for (int c = 0; c < min(3, nchunks); ++c) {
+                load_chunk(c);
+                last = c;
+            }
         for (int c = 0; c < nchunks; ++c) {
             if (c + 2 < nchunks) {
                 bar_sync(kBarEmpty + (c & 1), NTALL + NTX);  // inputs[c % 3] consumed
-                if (c + 3 < nchunks && lane == 0) load_chunk(c + 3);
+                if (c + 3 < nchunks && lane == 0 && !*abort) {
+                    load_chunk(c + 3);
+                    last = c + 3;
+                }
             }
             bar_sync(kBarStore, NTC + NTX);  // chunk c's output (and checkpoint) boxes staged
-            if (lane == 0) store_chunk(c);
+            if (lane == 0 && !*abort) store_chunk(c);
             if (c + 1 < nchunks) {
                 if (lane == 0) bulk_wait_read();
                 __syncwarp();
                 bar_arrive(kBarStoreFree, NTC + NTX);  // the checkpoint box and O[c & 1] free again
             }
         }
-        if (lane == 0) bulk_wait();
+        if (lane == 0) {
+            bulk_wait();
+            // every copy issued has landed before the CTA's shared memory is released (bounded)
+            for (int b = 0; b < 3 && b <= last; ++b)  // barrier b took chunks b, b + 3, ..., its last one
+                mbar_drain(&mbar[b], (unsigned)(((last - b) / 3) & 1));
+        }
         return;
     }
 
@@ -375,8 +392,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
             if (c + 1 < nchunks) issue(c + 1);
             cp_async_commit();
             cp_async_wait<1>();
-            if (!mbar_wait(&mbar[kb], (unsigned)((c / 3) & 1), kWaitTries) && lane == 0)
-                atomicAdd(&g_prefill_wait_timeouts, 1u);
+            mbar_wait_guarded(&mbar[kb], (unsigned)((c / 3) & 1), abort, &g_prefill_wait_timeouts);
             bar_sync(kBarPrep, NTP);
             const uint4 *cK = sK + kb * KH * BOXU, *cQ = sQ + kb * KH * BOXU;
             const float *sbeta = sGates[kb][0], *sgr = sGates[kb][1];
@@ -493,8 +509,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         const int p0 = c * C, nc = min(C, P - p0), pb = c & 1, kb = c % 3, ob = c & 1;
         bar_sync(kBarFull + pb, NTALL);
         // the inputs landed (already observed by the prep warps; re-checked, bounded)
-        if (!mbar_wait(&mbar[kb], (unsigned)((c / 3) & 1), kWaitTries) && lane == 0)
-            atomicAdd(&g_prefill_wait_timeouts, 1u);
+        mbar_wait_guarded(&mbar[kb], (unsigned)((c / 3) & 1), abort, &g_prefill_wait_timeouts);
         const uint4 *cK = sK + kb * KH * BOXU, *cQ = sQ + kb * KH * BOXU, *cV = sV + kb * VH * BOXU;
         uint4 *cO = sO + ob * VH * BOXU;
         const float *gam = sgam[pb], *dec = sdec[pb];
@@ -634,6 +649,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
         fence_proxy_async();
         bar_arrive(kBarStore, NTC + NTX);  // O boxes and checkpoint boxes staged for the producer
     }
+    if (*abort) return;  // a wait ran out: no results are stored
 #pragma unroll
     for (int mt = 0; mt < RT; ++mt)
 #pragma unroll

@@ -56,7 +56,6 @@ namespace {
 constexpr int kC = 64;            // tokens per chunk = checkpoint interval
 constexpr int kRoleThreads = 256; // 8 chain warps, then 8 prep warps
 constexpr int kTcThreads = 2 * kRoleThreads;
-constexpr int kTcTries = 1 << 22; // polls before a wait is reported as run out
 
 // tensor-memory columns (128 lanes each)
 constexpr uint32_t kColD1 = 0;    // [K; gam Q] S0^T, then + Mq delta; two chunk parities (2 x 128)
@@ -71,7 +70,9 @@ constexpr int kSolveThreads = 128;  // prep warps 8-11: the block solve
 // mbarriers
 constexpr int kMbLoad = 0;  // q/k of a stage (3)
 constexpr int kMbV = 3;     // v of a buffer (2)
-constexpr int kMbGram = 5, kMbC1 = 6, kMbC2 = 7, kMbC3 = 8, kMbC4 = 9, kNumMbar = 10;
+constexpr int kMbGram = 5, kMbC1 = 6, kMbC2 = 7, kMbC3 = 8, kMbC4 = 9;
+constexpr int kMbDrainChain = 10, kMbDrainPrep = 11;  // final drains of the two MMA issuers
+constexpr int kNumMbar = 12;
 
 // Shared memory (bytes). 128-byte-swizzled tiles start on 1024-byte boundaries.
 struct TcSmem {
@@ -94,6 +95,7 @@ struct TcSmem {
     static constexpr uint32_t kDec = kGam + 4 * kC * 4;        // fp32 [4][64]: e^{G_63 - G_s}
     static constexpr uint32_t kMbar = kDec + 4 * kC * 4;
     static constexpr uint32_t kTslot = kMbar + kNumMbar * 8;
+    static constexpr uint32_t kAbort = kTslot + 8;  // int: a wait ran out
     static constexpr uint32_t kBytes = kTslot + 16;
 };
 static_assert(TcSmem::kV == 3 * TcSmem::kStage && TcSmem::kCk == TcSmem::kV + 2 * TcSmem::kVBuf, "layout");
@@ -108,8 +110,11 @@ struct TcMaps {
     CUtensorMap q, k, v, o, ck;
 };
 
-__device__ __forceinline__ void tc_wait(unsigned long long *mb, unsigned parity, int lane) {
-    if (!mbar_wait(mb, parity, kTcTries) && lane == 0) atomicAdd(&g_prefill_tc_timeouts, 1u);
+// Bounded wait (kWaitBudgetNs). When one runs out, the CTA's abort flag goes up: from then on
+// no copies or global stores are issued, every role still passes its named barriers to the
+// end of its loop, the copies and MMAs issued are drained (bounded) and the CTA exits.
+__device__ __forceinline__ void tc_wait(unsigned long long *mb, unsigned parity, volatile int *abort) {
+    mbar_wait_guarded(mb, parity, abort, &g_prefill_tc_timeouts);
 }
 
 // 16-byte chunk `ch` of row `r` in a 64-row tile of 128-byte rows (128-byte swizzle), in uint4 units.
@@ -141,6 +146,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
     float(*sAjj)[16][16] = reinterpret_cast<float(*)[16][16]>(smem + L::kAjj);
     unsigned long long *mb = reinterpret_cast<unsigned long long *>(smem + L::kMbar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::kTslot);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + L::kAbort);
 
     const int h = blockIdx.x % H, n = blockIdx.x / H;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -152,6 +158,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
 
     if (tid == 0) {
         for (int i = 0; i < kNumMbar; ++i) mbar_init(&mb[i], 1);
+        *abort = 0;
         fence_proxy_async();
     }
     if (warp == 0) tmem_alloc<kTmemCols>(tslot);
@@ -212,7 +219,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
         // Prep warps on lane quarters 0-1 (8, 9, 12, 13: the K warps) read the K rows of the grams
         // (A), those on quarters 2-3 (10, 11, 14, 15: the Q warps) the Q rows (Mq).
         auto grams = [&](int c) {  // warp 14: the grams MMA of chunk c once its k, q have landed
-            tc_wait(&mb[kMbLoad + c % 3], (unsigned)((c / 3) & 1), lane);
+            tc_wait(&mb[kMbLoad + c % 3], (unsigned)((c / 3) & 1), abort);
             tc_fence_after();
             if (lane == 0) {  // [K;Q] (128 rows) x K^T
                 unsigned char *sKc = smem + L::kKQ + (c % 3) * L::kStage;
@@ -238,7 +245,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
             unsigned char *sK = smem + L::kKQ + s * L::kStage;
             if (c >= 2) bar_sync(kBEmpty + p, kTcThreads);  // the chain is done with chunk c-2 (Mq of parity p)
             bar_sync(kBPrep, kRoleThreads);                 // gates of chunk c written
-            tc_wait(&mb[kMbGram], (unsigned)p, lane);
+            tc_wait(&mb[kMbGram], (unsigned)p, abort);
             tc_fence_after();
             {   // row `row` of [K;Q] K^T, columns 32 half .. +31 (blocks b = 2 half, 2 half + 1 of 16 tokens).
                 // Decay e^{G_t - G_s}: direct inside t's block; across blocks e^{G_t - G_end(b)} e^{G_end(b) - G_s},
@@ -408,6 +415,10 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
                 }
             }
         }
+        if (pt == 6 * 32) {  // warp 14 issued the grams: they have completed before tensor memory is released
+            umma_commit(&mb[kMbDrainPrep]);
+            mbar_drain(&mb[kMbDrainPrep], 0u);
+        }
     } else {
         // ================================ chain ================================
         // Token-major halves: warps on lane quarters 0-1 ("lo") hold the K rows (R, delta), warps on
@@ -415,8 +426,10 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
         const bool lo = (warp & 3) < 2;
         const int t = 32 * (warp & 1) + lane;
         uint4 *rrow = reinterpret_cast<uint4 *>(smem + L::kR + half * 8192 + t * 128);
+        int last_qk = -1, last_v = -1;  // the last chunks whose copies were issued (thread 64), in order
         auto load_qk = [&](int c) {  // k, q boxes of chunk c into stage c % 3
             const int s = c % 3;
+            last_qk = c;
             unsigned char *st = smem + L::kKQ + s * L::kStage;
             mbar_arrive_expect_tx(&mb[kMbLoad + s], 4 * 8192);
             for (int x = 0; x < 2; ++x) {
@@ -426,6 +439,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
         };
         auto load_v = [&](int c) {  // v boxes of chunk c into buffer c & 1
             const int b = c & 1;
+            last_v = c;
             mbar_arrive_expect_tx(&mb[kMbV + b], 2 * 8192);
             for (int x = 0; x < 2; ++x)
                 tma_load_4d(smem + L::kV + b * L::kVBuf + x * 8192, &maps.v, 64 * x, h, c * kC, n, &mb[kMbV + b]);
@@ -450,13 +464,13 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
                              desc_kmajor(smem_addr(smem + L::kCk + (ks >> 2) * 16384) + (ks & 3) * 32), id, ks > 0);
                 umma_commit(&mb[kMbC1]);
             }
-            if (tid == 64 && c + 2 < nchunks) load_qk(c + 2);  // into the stage of chunk c-1, done with in both roles
+            if (tid == 64 && c + 2 < nchunks && !*abort) load_qk(c + 2);  // into the stage of chunk c-1, done with in both roles
             // Completion of this commit covers every earlier MMA too: delta of chunk c-1 has been read.
-            tc_wait(&mb[kMbC1], (unsigned)p, lane);
+            tc_wait(&mb[kMbC1], (unsigned)p, abort);
             tc_fence_after();
             if (lo) {  // R = V - gam_t (K S0^T)_t -> fp16 operand tile [t][dv]
                 const float gt = sGam[c % 4][t];
-                tc_wait(&mb[kMbV + p], (unsigned)((c >> 1) & 1), lane);
+                tc_wait(&mb[kMbV + p], (unsigned)((c >> 1) & 1), abort);
                 const uint4 *vrow = reinterpret_cast<const uint4 *>(vb + half * 8192 + t * 128);
                 uint4 vv[8];  // this row's v, chunk j = dv 64 half + 8 j ..
 #pragma unroll
@@ -493,9 +507,9 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
             }
             if (tid == 64 && c >= 1) {
                 bulk_wait_read();                      // the stores of chunk c-1 have read its output rows and the carry
-                if (c + 1 < nchunks) load_v(c + 1);    // into the buffer of chunk c-1
+                if (c + 1 < nchunks && !*abort) load_v(c + 1);  // into the buffer of chunk c-1
             }
-            tc_wait(&mb[kMbC2], (unsigned)p, lane);
+            tc_wait(&mb[kMbC2], (unsigned)p, abort);
             tc_fence_after();
             if (c + 1 < nchunks) bar_arrive(kBTFree, kRoleThreads + kSolveThreads);  // T read
             if (lo) {  // delta rows -> fp16 operand tile (over R); dec_t delta_t -> the v buffer
@@ -531,12 +545,12 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
                              desc_mnmajor(smem_addr(smem + L::kR) + ks * 2048, 8192), ido, true);
                 umma_commit(&mb[kMbC4]);
             }
-            tc_wait(&mb[kMbC3], (unsigned)p, lane);
+            tc_wait(&mb[kMbC3], (unsigned)p, abort);
             tc_fence_after();
             {   // S64 = gam_63 S0 + (dec delta)^T K, row dv = `row`, dk 64 half .. +63: new carry (fp16),
                 // checkpoint, final state
                 const float gl = sGam[c % 4][kC - 1];
-                __half *so = (c + 1 == nchunks) ? s_out + set_off + (size_t)row * 128 : nullptr;
+                __half *so = (c + 1 == nchunks && !*abort) ? s_out + set_off + (size_t)row * 128 : nullptr;
                 uint4 *crow = reinterpret_cast<uint4 *>(smem + L::kCk + half * 16384 + row * 128);
                 uint4 cv[8];  // this row's carry, chunk lq = dk 64 half + 8 lq ..
 #pragma unroll
@@ -567,7 +581,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
             tc_fence_before();
             bar_sync(kBChain, kRoleThreads);
             if (!lo) {  // output rows O_t = (gam Q S0^T + Mq delta)_t -> v buffer [t][dv] -> TMA store
-                tc_wait(&mb[kMbC4], (unsigned)p, lane);
+                tc_wait(&mb[kMbC4], (unsigned)p, abort);
                 tc_fence_after();
                 uint4 *orow = reinterpret_cast<uint4 *>(vb + half * 8192 + t * 128);
 #pragma unroll
@@ -579,7 +593,7 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
                 fence_proxy_async();
                 tc_fence_before();
                 bar_sync(kBOut, kRoleThreads / 2);
-                if (tid == 64) {  // at a full chunk the carry tile is the checkpoint
+                if (tid == 64 && !*abort) {  // at a full chunk the carry tile is the checkpoint
                     if (nc == kC)
                         for (int x = 0; x < 2; ++x)
                             tma_store_3d(&maps.ck, 64 * x, 0, (n * nfull + c) * H + h, smem + L::kCk + x * 16384);
@@ -598,7 +612,18 @@ prefill_tc_kernel(int H, int P, const __grid_constant__ TcMaps maps, const float
                 *reinterpret_cast<uint4 *>(s_out + set_off + (size_t)row * 128 + ch * 8) = u;
             }
         }
-        if (tid == 64) bulk_wait();
+        if (tid == 64) {
+            bulk_wait();
+            // every copy issued has landed before the CTA's shared memory is released (bounded)
+            for (int b = 0; b < 3 && b <= last_qk; ++b)  // stage b took chunks b, b + 3, ...
+                mbar_drain(&mb[kMbLoad + b], (unsigned)(((last_qk - b) / 3) & 1));
+            for (int b = 0; b < 2 && b <= last_v; ++b)   // buffer b took chunks b, b + 2, ...
+                mbar_drain(&mb[kMbV + b], (unsigned)(((last_v - b) / 2) & 1));
+        }
+        if (tid == 0) {  // every MMA this thread issued has completed before tensor memory is released
+            umma_commit(&mb[kMbDrainChain]);
+            mbar_drain(&mb[kMbDrainChain], 0u);
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -365,27 +365,37 @@ dn_status dn_prefix_cache_lookup(dn_prefix_cache *c, const int32_t *tokens, int 
 int dn_prefix_cache_size(dn_prefix_cache *c);
 
 /*
- * dn_prefill_wait_timeouts -- diagnostics of the fp16 prefill kernel.
+ * dn_prefill_wait_timeouts -- diagnostics of the fp16 prefill kernels.
  *
- * The fp16 prefill streams its inputs with the GPU's tensor-copy engine and waits
- * for them with bounded polls; a wait that runs out is counted (never a hang), and
- * the results of that call are invalid. Returns how many waits ran out since the
- * library was loaded on the current device (0 in correct operation), or
- * 0xffffffff if the counter could not be read. Synchronises the current device.
+ * The fp16 prefill kernels stream their inputs with the GPU's tensor-copy engine and
+ * hand work between warp roles on shared-memory barriers. Every such wait is bounded
+ * in time: it gives up after 1 second (1,000,000 us; a wait lasts a few microseconds
+ * when the work it waits for progresses). When one runs out, the CTA counts the failure
+ * here once, stops issuing copies and global stores, waits at most the same budget for
+ * the copies and tensor-core operations it has already issued, and exits; the results
+ * of that call are then invalid, and nothing hangs. Returns how many CTAs gave up since
+ * the library was loaded on the current device (0 in correct operation), or 0xffffffff
+ * if the counter could not be read. Synchronises the current device.
  */
 unsigned int dn_prefill_wait_timeouts(void);
 
 /*
- * dn_wait_selftest -- checks on the device the bounded wait the prefill kernels use.
+ * dn_wait_selftest -- checks on the device the bounded waits of the prefill kernels.
  *
- * Launches one small kernel on `stream` that waits, with at most `tries` polls, on a
- * shared-memory barrier nothing has arrived on, then arrives once and waits again.
- * Writes result[0] = 1 if the first wait gave up (as it must), result[1] = 1 if the
- * second returned (as it must). result: 2 int32 in device memory, 4-byte aligned, owned by
- * the caller. 1 <= tries <= 2^20 (the kernel ends within microseconds at 1000 polls).
- * Errors: DN_ERR_INVALID_ARG (nothing launched), DN_ERR_CUDA (launch failed).
+ * Launches one small kernel on `stream` that uses the kernels' own wait functions with a
+ * time budget of `budget_us` microseconds:
+ *   result[0] = 1: a wait on a shared-memory barrier nothing arrives on gave up after the
+ *                  budget and raised the CTA's abort flag;
+ *   result[1] = 1: after the one expected arrival, the same wait returned;
+ *   result[2] = 1: the drain path: a 16-byte bulk copy from result[0..3] into shared memory
+ *                  was in flight when a second wait ran out; the drain waited for it and
+ *                  the copy landed with the bytes result[0..3] held at the launch;
+ *   result[3] = 2: each of the two failures was counted once.
+ * result: 4 int32 in device memory, 16-byte aligned, owned by the caller; its first 16
+ * bytes are also the copy's source. 1 <= budget_us <= 1,000,000; the kernel takes about
+ * two budgets. Errors: DN_ERR_INVALID_ARG (nothing launched), DN_ERR_CUDA (launch failed).
  */
-dn_status dn_wait_selftest(int tries, int32_t *result, dn_stream_t stream);
+dn_status dn_wait_selftest(int budget_us, int32_t *result, dn_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char *dn_status_string(dn_status s);

@@ -108,3 +108,24 @@ def test_one_layer_launch_matches_folded_launch_and_oracle(T, cuda):
                                        np64(x["state"][0:1, heads]), store="f16", io="f16")
     assert_close("out", out[0:1, :, heads], o_ref, TOL["f16"])
     assert_close("ckpt", ckpt[0:1, :, heads], c_ref, TOL["f16"])
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_short_blocks_in_large_launches_match_one_layer_launches(T, cuda):
+    # Blocks of up to 8 tokens over many state sets run as 32-row CTAs with the 8-token tile
+    # capacity; one set at a time runs as 16-row CTAs. The arithmetic per state row is the
+    # same, so the results are bit-identical, and a sample matches the oracle.
+    N, H, d = 8, 16, 128
+    x = inputs.recurrence_inputs(N, T, H, d, d, seed=60 + T, device=cuda)
+    out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    for n in (0, 5, 7):
+        sl = {k: x[k][n:n + 1] for k in ("q", "k", "v", "beta", "g", "state")}
+        o1, c1 = dn.dn_verify_block(sl["q"], sl["k"], sl["v"], sl["beta"], sl["g"], sl["state"])
+        torch.cuda.synchronize()
+        assert torch.equal(o1[0], out[n]) and torch.equal(c1[0], ckpt[n]), n
+    heads = [1, 9, 15]
+    u = {k: np64(x[k][2:4, :, heads]) for k in ("q", "k", "v", "beta", "g")}
+    o_ref, c_ref = oracle.verify_block(u["q"], u["k"], u["v"], u["beta"], u["g"],
+                                       np64(x["state"][2:4][:, heads]), store="f16", io="f16")
+    assert_close("out", out[2:4][:, :, heads], o_ref, TOL["f16"])
+    assert_close("ckpt", ckpt[2:4][:, :, heads], c_ref, TOL["f16"])

@@ -15,6 +15,7 @@
 #include "dn.h"
 #include "dn_device.cuh"
 #include "dn_internal.h"
+#include "dn_mma.cuh"
 #include "dn_recurrence.cuh"
 
 namespace dn {
@@ -53,28 +54,41 @@ commit_kernel(int B, int T, unsigned pieces, size_t set_bytes, const uint4 *__re
 // ---------------------------------------------------------------------------------------
 // Recompute on commit. dn_verify_block_deltas keeps no per-position states; it writes
 // delta_t = beta_t (v_t - g_t S_{t-1} k_t) for every position, and the accepted state is
-// S_a = g_{a-1} ( ... (g_0 S_0 + delta_0 k_0^T) ... ) + delta_{a-1} k_{a-1}^T, applied here
-// to the old state in place with exactly the arithmetic (packed fp32x2 FMAs in the same
-// order) the checkpoint path uses, so both paths commit bit-identical states.
-// A CTA owns 64 rows of one (state set, head): warp w the rows 8w .. 8w+7, lane l the DK/32
-// columns from l DK/32 in all of them. Per step a lane reads its columns of k_t once from
-// shared memory (distinct addresses across the warp: no quarter-warp pass repeats another)
-// and reuses them for its eight rows; delta and the gate are broadcasts. (With eight lanes
-// per row, each 16-byte read of k served four rows of a warp in four separate quarter-warp
-// passes, and the shared-memory pipe, not HBM, bounded the kernel; with four rows per warp
-// the shared reads and loop overhead, not the packed FMAs, still made up most of the
-// instructions.)
+// S_a = g_{a-1} ( ... (g_0 S_0 + delta_0 k_0^T) ... ) + delta_{a-1} k_{a-1}^T
+//     = Gam S_0 + D^T K,   Gam = g_0 ... g_{a-1},  D[s][i] = (g_{s+1} ... g_{a-1}) delta_s[i]
+// with K the a accepted keys. D^T K is one rank-a product per 64-row block of the state, on
+// the tensor cores: tf32 MMAs (m16n8k8) with D split into a tf32 high part and the tf32 of
+// the remainder, so the product keeps about 22 bits of D (k is fp16, exact in tf32) and the
+// fp32 range. The sum is as accurate as the token-by-token replay but in another order, so the
+// committed state can differ from dn_verify_block + dn_commit in the last fp16 bit.
+// A CTA owns 64 rows of one (state set, head): the rows go through shared memory (16-byte
+// loads and stores, 16-byte chunks swizzled by row so the fragment reads are conflict free);
+// warp w computes rows 16 (w / 2) .. +15 and half of the dk columns.
 constexpr int kDeltaRows = 64;
 
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 template <int DK>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256, 5)
 commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
                      const float *__restrict__ g, const float *__restrict__ delta,
                      const int *__restrict__ accepted, __half *__restrict__ state) {
-    constexpr int ROWS = kDeltaRows, RPW = ROWS / 8, CPL = DK / 32, NP = CPL / 2;
-    static_assert(CPL == 2 || CPL == 4, "two or four columns per lane");
-    __shared__ __align__(16) float sk[DN_MAX_BLOCK][DK];
-    __shared__ float sd[DN_MAX_BLOCK][ROWS], sg[DN_MAX_BLOCK];
+    constexpr int ROWS = kDeltaRows, CPR = DK / 8, NTW = DK / 16;  // 16-byte chunks per row; n-tiles per warp
+    __shared__ __align__(16) uint4 sS[ROWS * CPR];                  // the state rows, fp16
+    __shared__ __align__(16) __half sK[DN_MAX_BLOCK][DK + 8];       // the accepted keys (zeros past a)
+    __shared__ float sD[DN_MAX_BLOCK][ROWS + 8];                    // D[s][row] (zeros past a)
+    __shared__ float sgate[DN_MAX_BLOCK + 1];  // decay of each position, then Gam
     const int rblocks = DV / ROWS;
     const int rb = blockIdx.x % rblocks;
     const int h = (blockIdx.x / rblocks) % H;
@@ -84,67 +98,91 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
     const int a = __ldg(&accepted[n % B]);
     if (a < 1 || a > T) return;  // a == 0: keep the state; out of range: ignored
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    __half *sp = state + ((n * H + h) * (size_t)DV + rb * ROWS + warp * RPW) * DK + lane * CPL;
+    const int gid = lane >> 2, t4 = lane & 3;
+    uint4 *sp = reinterpret_cast<uint4 *>(state + ((n * H + h) * (size_t)DV + rb * ROWS) * DK);
 
-    float2 s[RPW][NP];  // rows 4w + r, columns lane CPL + 2p, + 1
+    // The state rows (chunk c of row r at c ^ (r & 7)) and the keys (zeros past a) go in by
+    // cp.async first; they are not needed before the MMA (keys) and the epilogue (rows), so
+    // their latency overlaps the gates and D below.
+    for (int i = tid; i < ROWS * CPR; i += 256) {
+        const int r = i / CPR, c = i % CPR;
+        cp_async16(&sS[r * CPR + (c ^ (r & 7))], sp + i, 16);
+    }
+    for (int i = tid; i < DN_MAX_BLOCK * (DK / 8); i += 256) {
+        const int s2 = i / (DK / 8), j8 = i % (DK / 8);
+        const bool live = s2 < a;
+        cp_async16(&sK[s2][8 * j8], live ? (const void *)(k + ((n * T + s2) * H + h) * DK + (size_t)j8 * 8) : (const void *)k,
+                   live ? 16 : 0);
+    }
+    cp_async_commit();
+    // decay of position s: g_{s+1} ... g_{a-1} (suffix products, one warp), and Gam = g_0 ... g_{a-1}
+    if (warp == 0) {
+        float gt = lane < a ? __ldg(&g[(n * T + lane) * H + h]) : 1.f;
+        float suf = gt;  // inclusive suffix product over lanes >= this one, then shifted by one
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        __half2 hv[NP];
-        if constexpr (NP == 2) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(sp + (size_t)r * DK);
-            hv[0] = *reinterpret_cast<const __half2 *>(&u.x);
-            hv[1] = *reinterpret_cast<const __half2 *>(&u.y);
-        } else {
-            hv[0] = *reinterpret_cast<const __half2 *>(sp + (size_t)r * DK);
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf *= o;
         }
-#pragma unroll
-        for (int p = 0; p < NP; ++p) s[r][p] = __half22float2(hv[p]);
+        const float excl = __shfl_down_sync(0xffffffffu, suf, 1);
+        if (lane < DN_MAX_BLOCK) sgate[lane] = lane + 1 < 32 ? excl : 1.f;
+        if (lane == 0) sgate[DN_MAX_BLOCK] = suf;  // the product of every gate: Gam
     }
-    for (int i = tid; i < a * (DK / 8); i += 256) {
-        const int t = i / (DK / 8), j8 = i % (DK / 8);
-        float x[8];
-        load8(k + ((n * T + t) * H + h) * DK + (size_t)j8 * 8, x);
-        *reinterpret_cast<float4 *>(&sk[t][8 * j8]) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4 *>(&sk[t][8 * j8 + 4]) = make_float4(x[4], x[5], x[6], x[7]);
-    }
-    for (int i = tid; i < a * ROWS; i += 256) {
-        const int t = i / ROWS, r = i % ROWS;
-        sd[t][r] = delta[((n * T + t) * H + h) * DV + rb * ROWS + r];
-    }
-    if (tid < a) sg[tid] = g[(n * T + tid) * H + h];
     __syncthreads();
-    for (int t = 0; t < a; ++t) {
-        const float gt = sg[t];
-        const float2 g2 = make_float2(gt, gt);
-        float2 kf[NP];
-        if constexpr (NP == 2) {
-            const float4 k4 = *reinterpret_cast<const float4 *>(&sk[t][lane * CPL]);
-            kf[0] = make_float2(k4.x, k4.y);
-            kf[1] = make_float2(k4.z, k4.w);
-        } else {
-            kf[0] = *reinterpret_cast<const float2 *>(&sk[t][lane * CPL]);
+    // D[s][row] = decay_s delta_s[row], zeros past a
+    for (int i = tid; i < DN_MAX_BLOCK * ROWS; i += 256) {
+        const int s2 = i / ROWS, r = i % ROWS;
+        sD[s2][r] = s2 < a ? sgate[s2] * __ldg(&delta[((n * T + s2) * H + h) * DV + rb * ROWS + r]) : 0.f;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    const float gam = sgate[DN_MAX_BLOCK];
+
+    // this warp's rows, and its n-tiles in groups of four (four accumulators of four floats)
+    const int m0 = 16 * (warp >> 1), nt0 = (warp & 1) * NTW;
+    __half *sh = reinterpret_cast<__half *>(sS);
+#pragma unroll 1
+    for (int j0 = 0; j0 < NTW; j0 += 4) {
+        float acc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            if (8 * ks >= a) break;
+            const float x[4] = {sD[8 * ks + t4][m0 + gid], sD[8 * ks + t4][m0 + gid + 8],
+                                sD[8 * ks + t4 + 4][m0 + gid], sD[8 * ks + t4 + 4][m0 + gid + 8]};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                hi[e] = to_tf32(x[e]);
+                lo[e] = to_tf32(x[e] - __uint_as_float(hi[e]));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = 8 * (nt0 + j0 + j) + gid;
+                const uint32_t b[2] = {__float_as_uint(__half2float(sK[8 * ks + t4][col])),
+                                       __float_as_uint(__half2float(sK[8 * ks + t4 + 4][col]))};
+                mma_tf32(acc[j], hi, b);
+                mma_tf32(acc[j], lo, b);
+            }
         }
+        // S_a = Gam S_0 + D^T K, rounded to fp16, back into the rows in shared memory
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const float dt = sd[t][warp * RPW + r];
-            const float2 d2 = make_float2(dt, dt);
+        for (int j = 0; j < 4; ++j) {
+            const int col = 8 * (nt0 + j0 + j) + 2 * t4;
 #pragma unroll
-            for (int p = 0; p < NP; ++p) s[r][p] = __ffma2_rn(d2, kf[p], __fmul2_rn(g2, s[r][p]));
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = m0 + gid + 8 * hh;
+                __half2 *p = reinterpret_cast<__half2 *>(sh + r * DK + (((col >> 3) ^ (r & 7)) << 3) + (col & 7));
+                const float2 s0 = __half22float2(*p);
+                *p = __floats2half2_rn(fmaf(gam, s0.x, acc[j][2 * hh]), fmaf(gam, s0.y, acc[j][2 * hh + 1]));
+            }
         }
     }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        __half2 hv[NP];
-#pragma unroll
-        for (int p = 0; p < NP; ++p) hv[p] = __float22half2_rn(s[r][p]);
-        if constexpr (NP == 2) {
-            uint2 u;
-            u.x = *reinterpret_cast<const unsigned *>(&hv[0]);
-            u.y = *reinterpret_cast<const unsigned *>(&hv[1]);
-            *reinterpret_cast<uint2 *>(sp + (size_t)r * DK) = u;
-        } else {
-            *reinterpret_cast<__half2 *>(sp + (size_t)r * DK) = hv[0];
-        }
+    __syncthreads();
+    for (int i = tid; i < ROWS * CPR; i += 256) {
+        const int r = i / CPR, c = i % CPR;
+        __stcs(sp + i, sS[r * CPR + (c ^ (r & 7))]);
     }
 }
 

@@ -130,9 +130,14 @@ dn_status dn_verify_block(int N, int H, int T, int dk, int dv,
  *   delta_t = beta_t (v_t - g_t S_{t-1} k_t)        (one fp32 per state row)
  *
  * so that S_t = g_t S_{t-1} + delta_t k_t^T; commit then rebuilds the accepted state
- * S_a from the old state, delta_0..delta_{a-1}, k and g, in place. The committed state
- * is bit-identical to dn_verify_block + dn_commit on the same inputs; out is identical
- * to dn_verify_block's.
+ * in place from the old state, delta_0..delta_{a-1}, k and g, in closed form:
+ *
+ *   S_a = (g_0 ... g_{a-1}) S_0 + sum_{s<a} (g_{s+1} ... g_{a-1}) delta_s k_s^T
+ *
+ * (one small tensor-core product per 64 state rows, with fp32-level accuracy). out is
+ * identical to dn_verify_block's. The committed state agrees with dn_verify_block +
+ * dn_commit on the same inputs to within one fp16 unit in the last place, and is equal
+ * for nearly every element: both sum in fp32, in different orders.
  *
  * dn_verify_block_deltas: arguments as dn_verify_block, with
  *   delta    [N][T][H][dv] fp32, 16-byte aligned, written (instead of ckpt)

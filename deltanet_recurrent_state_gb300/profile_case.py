@@ -1,6 +1,6 @@
 """Run one libdn kernel on a small case for profiling (a few launches, inputs > L2).
 
-    python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3] [--T 16]
+    python -m deltanet_recurrent_state_gb300.profile_case verify  [--layers 8] [--launches 3] [--T 16] [--per-layer]
     python -m deltanet_recurrent_state_gb300.profile_case accept  [--requests 128]
     python -m deltanet_recurrent_state_gb300.profile_case commit  [--layers 48]
     python -m deltanet_recurrent_state_gb300.profile_case prefill [--tokens 4096] [--sequences 1] [--engine mma|tc]
@@ -35,6 +35,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--engine", choices=["mma", "tc"], default="mma", help="prefill engine")
     ap.add_argument("--T", type=int, default=16, help="verify block width (accept: positions per request)")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="verify: each pass is one launch per layer (N = 1) instead of one over all layers")
     a = ap.parse_args()
     dev = torch.device("cuda:0")
     H, d, T, V = 48, 128, a.T, 151936
@@ -43,7 +45,11 @@ def main():
         out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
         acc = torch.full((1,), T - 1, dtype=torch.int32, device=dev)
         for _ in range(a.warmup + a.launches):
-            if a.kernel == "verify":
+            if a.kernel == "verify" and a.per_layer:
+                for l in range(a.layers):
+                    dn.dn_verify_block(x["q"][l:l + 1], x["k"][l:l + 1], x["v"][l:l + 1], x["beta"][l:l + 1],
+                                       x["g"][l:l + 1], x["state"][l:l + 1], out[l:l + 1], ckpt[l:l + 1])
+            elif a.kernel == "verify":
                 dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], out, ckpt)
             else:
                 dn.dn_commit(ckpt, acc, x["state"])

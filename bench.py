@@ -606,7 +606,54 @@ def verify_per_layer_row(sets, device, stream, reps=50, warmup=5):
     for name in ("per_layer", "folded"):
         res[name]["frac"] = res[name]["gbs"] / hbm
     res["bytes_per_layer_launch"] = verify_bytes(1, T, H, dk, dv, 2)
-    res["ctas_per_layer_launch"] = H * dv // 32
+    # 32-row CTAs, or 16-row ones when a launch has fewer 32-row CTAs than two per SM
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    res["ctas_per_layer_launch"] = H * dv // 32 if H * dv // 32 >= 2 * sms else H * dv // 16
+    return res
+
+
+def commit_alone_row(sets, device, stream, reps=20, warmup=3):
+    """dn_commit of the single-user step (48 state sets, T = 16) timed by itself, in two
+    conditions: after an L2 flush (a 512 MB read), and right after the step's verify (its
+    checkpoint stores leave up to an L2's worth of dirty lines, written back while commit
+    runs). The first is the copy's own rate; the second is what it costs inside the step."""
+    import torch
+    from deltanet_recurrent_state_gb300 import binding as dn
+    from deltanet_recurrent_state_gb300.workloads import WORKLOADS
+    w = WORKLOADS[HEADLINE]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    flush.fill_(1.0)
+    sink = torch.empty((), dtype=torch.float32, device=device)
+    with torch.cuda.stream(stream):
+        for x in sets:  # targets and accepted lengths of every set
+            dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+    torch.cuda.synchronize()
+    res = {"workload": HEADLINE + " commit"}
+    for cond in ("after_l2_flush", "after_verify"):
+        times, nbytes = [], []
+        for i in range(warmup + reps):
+            x = sets[i % len(sets)]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                if cond == "after_l2_flush":
+                    torch.sum(flush, out=sink)
+                else:
+                    dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                                       x["ckpt"], stream=stream)
+                e0.record(stream)
+                dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                times.append(e0.elapsed_time(e1))
+                nbytes.append(commit_bytes(w["L"], x["acc_plan"], w["H"], w["dk"], w["dv"], 2))
+        ms = statistics.median(times)
+        gbs = statistics.mean(nbytes) / (ms / 1e3) / 1e9
+        res[cond] = {"us": ms * 1e3, "gbs": gbs}
+    hbm, _ = peaks()
+    for cond in ("after_l2_flush", "after_verify"):
+        res[cond]["frac"] = res[cond]["gbs"] / hbm
+    del flush
     return res
 
 
@@ -839,6 +886,7 @@ def main():
     rows = {}
     if not args.no_rows and rank == 0:
         rows["verify_per_layer"] = verify_per_layer_row(sets, device, stream)
+        rows["commit_alone"] = commit_alone_row(sets, device, stream)
         rows["recompute_on_commit_step"] = deltas_row(sets, device, stream)
         rows["decode_loop"] = decode_row(device, stream)
         rows["batch64_step"] = batch_row(device, stream)

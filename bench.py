@@ -636,7 +636,7 @@ def commit_alone_row(sets, device, stream, reps=20, warmup=3):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
                 if cond == "after_l2_flush":
-                    torch.sum(flush, out=sink)
+                    torch.sum(flush, dim=0, out=sink)
                 else:
                     dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
                                        x["ckpt"], stream=stream)

@@ -363,6 +363,10 @@ constexpr int kTpr = 8;
 // registers, and the head's state-independent work is shared by twice the rows (a whole head
 // per CTA measured slower again).
 constexpr int kWyRowsCkpt = 32, kWyRowsCkptSmall = 16, kWyRowsDelta = 64;
+// Blocks of up to kWyShortBlock tokens in large launches: 64-row CTAs, so the head's prologue
+// (k/q tiles, grams, gates, L and M) is shared by twice the rows against only a few
+// checkpoint stores per row.
+constexpr int kWyRowsCkptShort = 64, kWyShortBlock = 4;
 
 template <int DK, bool CKPT, int TM, int R>
 void launch_verify_wy_rows(int N, int H, int T, int dv, const __half *q, const __half *k, const __half *v,
@@ -379,16 +383,25 @@ void launch_verify_wy(int N, int H, int T, int dv, const __half *q, const __half
                       float *delta, cudaStream_t st) {
     if constexpr (!CKPT) {
         launch_verify_wy_rows<DK, CKPT, TM, kWyRowsDelta>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta, st);
-    } else if constexpr (DK == 128) {
-        // fewer 32-row CTAs than two per SM: the 16-row CTAs spread the stores evenly
-        const long long ctas32 = (long long)N * H * (dv / kWyRowsCkpt);
-        if (ctas32 < 2LL * device_sm_count())
-            launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkptSmall>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt,
-                                                                  delta, st);
-        else
-            launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkpt>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta,
-                                                             st);
+        return;
     } else {
+        const long long ctas32 = (long long)N * H * (dv / kWyRowsCkpt);
+        const bool few = ctas32 < 2LL * device_sm_count();
+        if constexpr (DK == 128) {
+            // fewer 32-row CTAs than two per SM: the 16-row CTAs spread the stores evenly
+            if (few) {
+                launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkptSmall>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt,
+                                                                      delta, st);
+                return;
+            }
+        }
+        if constexpr (TM == 8) {
+            if (!few && T <= kWyShortBlock) {
+                launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkptShort>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt,
+                                                                      delta, st);
+                return;
+            }
+        }
         launch_verify_wy_rows<DK, CKPT, TM, kWyRowsCkpt>(N, H, T, dv, q, k, v, beta, g, s_in, out, ckpt, delta, st);
     }
 }

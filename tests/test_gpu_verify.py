@@ -112,9 +112,10 @@ def test_one_layer_launch_matches_folded_launch_and_oracle(T, cuda):
 
 @pytest.mark.parametrize("T", [1, 4, 8])
 def test_short_blocks_in_large_launches_match_one_layer_launches(T, cuda):
-    # Blocks of up to 8 tokens over many state sets run as 32-row CTAs with the 8-token tile
-    # capacity; one set at a time runs as 16-row CTAs. The arithmetic per state row is the
-    # same, so the results are bit-identical, and a sample matches the oracle.
+    # Blocks of up to 8 tokens over many state sets run with the 8-token tile capacity, as
+    # 64-row CTAs up to 4 tokens and 32-row CTAs above; one set at a time runs as 16-row CTAs.
+    # The arithmetic per state row is the same, so the results are bit-identical, and a
+    # sample matches the oracle.
     N, H, d = 8, 16, 128
     x = inputs.recurrence_inputs(N, T, H, d, d, seed=60 + T, device=cuda)
     out, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])

@@ -220,8 +220,32 @@ def make_step_sets(w, device, rank, count):
     return sets
 
 
-def run_step(x, stream, evs=None):
+def side_stream(device):
+    """A high-priority second stream: accept runs on it beside verify."""
+    import torch
+    lo, hi = torch.cuda.Stream.priority_range()
+    return torch.cuda.Stream(device=device, priority=hi)
+
+
+def run_step(x, stream, evs=None, side=None):
+    """One step: verify, accept, commit. With `side`, accept (which reads only the logits and
+    the draft ids) runs on the side stream concurrently with verify, and commit waits for
+    both; with `evs` (the per-kernel breakdown) the three run one after another with events
+    between them."""
+    import torch
     from deltanet_recurrent_state_gb300 import binding as dn
+    if side is not None and not evs:
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        side.wait_event(fork)
+        dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=side)
+        join = torch.cuda.Event()
+        join.record(side)
+        dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"], x["ckpt"],
+                           stream=stream)
+        stream.wait_event(join)
+        dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
+        return
     if evs:
         evs[0].record(stream)
     dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"], x["ckpt"],
@@ -238,21 +262,23 @@ def run_step(x, stream, evs=None):
 
 def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True):
     """Warm up, then time exactly `steps` steps between barriers; returns (seconds,
-    per-kernel mean ms [verify, accept, commit], wall-clock bounds). With `graphs`, each
-    buffer set's step (the three calls) is captured once in a CUDA graph and a timed step is
-    one replay, as a serving loop launches a fixed step; the per-kernel durations then come
-    from a separate eager pass with events recorded between the launches."""
+    per-kernel mean ms [verify, accept, commit], wall-clock bounds). Accept runs on a second
+    stream beside verify (run_step). With `graphs`, each buffer set's step (the three calls)
+    is captured once in a CUDA graph and a timed step is one replay, as a serving loop
+    launches a fixed step; the per-kernel durations then come from a separate eager pass with
+    the three launches one after another and events recorded between them."""
     import torch
+    side = side_stream(stream.device)
     with torch.cuda.stream(stream):
         for i in range(warmup):
-            run_step(sets[i % len(sets)], stream)
+            run_step(sets[i % len(sets)], stream, side=side)
     torch.cuda.synchronize()
     if graphs:
         gs = []
         for x in sets:
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr, stream=stream):
-                run_step(x, stream)
+                run_step(x, stream, side=side)
             gs.append(gr)
         with torch.cuda.stream(stream):
             for i in range(warmup):
@@ -262,7 +288,7 @@ def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True)
             gs[i % len(gs)].replay()
     else:
         def step(i):
-            run_step(sets[i % len(sets)], stream)
+            run_step(sets[i % len(sets)], stream, side=side)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist is not None:
@@ -370,7 +396,9 @@ def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
     h2d = host[0].numel()
     d2h = host_out[0].numel()
     copy_stream = torch.cuda.Stream(device=device)
+    side = side_stream(device)
     events = [[torch.cuda.Event() for _ in range(groups + 1)] for _ in sets]
+    joins = [torch.cuda.Event() for _ in sets]
 
     def body(j):
         x = dict(sets[j])
@@ -378,21 +406,24 @@ def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
         x.update(dev_out[j][1])
         if groups == 1:
             dev_in[j][0].copy_(host[j], non_blocking=True)  # one pinned copy (the host link's full rate)
+            side.wait_stream(stream)
         else:
             copy_stream.wait_stream(stream)
             with torch.cuda.stream(copy_stream):
                 for i, (a0, a1) in enumerate(segs):
                     dev_in[j][0][a0:a1].copy_(host[j][a0:a1], non_blocking=True)
                     events[j][i].record(copy_stream)
+            side.wait_event(events[j][groups])  # the logits and drafts have landed
+        # accept beside the verify calls (it reads only the logits and drafts)
+        dn.dn_accept_greedy(dvw["logits"], dvw["draft"], x["tgt"], x["acc"], x["ws"], stream=side)
+        joins[j].record(side)
         for gi in range(groups):
             if groups > 1:
                 stream.wait_event(events[j][gi])
             sl = slice(bounds[gi], bounds[gi + 1])
             dn.dn_verify_block(dvw["q%d" % gi], dvw["k%d" % gi], dvw["v%d" % gi], dvw["beta%d" % gi],
                                dvw["g%d" % gi], x["state"][sl], x["out"][sl], x["ckpt"][sl], stream=stream)
-        if groups > 1:
-            stream.wait_event(events[j][groups])
-        dn.dn_accept_greedy(dvw["logits"], dvw["draft"], x["tgt"], x["acc"], x["ws"], stream=stream)
+        stream.wait_event(joins[j])
         dn.dn_commit(x["ckpt"], x["acc"], x["state"], stream=stream)
         host_out[j].copy_(dev_out[j][0], non_blocking=True)
 
@@ -496,7 +527,21 @@ def deltas_row(sets, device, stream, steps=200, warmup=5):
     for x in sets:
         x["delta"] = torch.empty((N, T, H, dv), dtype=torch.float32, device=device)
 
+    side = side_stream(device)
+
     def step(x, evs=None):
+        if not evs:  # accept beside verify, commit after both (as run_step)
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            side.wait_event(fork)
+            dn.dn_accept_greedy(x["logits"], x["draft"], x["tgt"], x["acc"], x["ws"], stream=side)
+            join = torch.cuda.Event()
+            join.record(side)
+            dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
+                                      x["delta"], stream=stream)
+            stream.wait_event(join)
+            dn.dn_commit_deltas(x["k"], x["g"], x["delta"], x["acc"], x["state"], stream=stream)
+            return
         if evs:
             evs[0].record(stream)
         dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"], x["out"],
@@ -933,8 +978,10 @@ def main():
                    "l2": "inputs larger than L2 (%.2f GB per step), %d rotating buffer sets"
                          % ((vb + ab + cb) / 1e9, ROTATE),
                    "parallelism": "replicas" if world == 1 else "dp%d (independent requests)" % world,
-                   "launch": "one CUDA graph replay per step (the three calls); per-kernel "
-                             "durations from an eager pass with events between the launches"},
+                   "launch": "one CUDA graph replay per step: verify, accept beside it on a second "
+                             "stream (it reads only logits and drafts), then commit; per-kernel "
+                             "durations from an eager pass with the three launches one after "
+                             "another and events between them"},
         "roofline": {"bound": "hbm", "kernel": "dn_verify_block", "achieved": achieved,
                      "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                      "frac_of_nominal_8tbs": achieved / 8000.0, "traffic": traffic,
@@ -950,9 +997,10 @@ def main():
                 "d2h_bytes_per_step": d2h, "steps": e2e_k,
                 "how": "one CUDA graph replay per step: the inputs of layer groups of %s layers go "
                        "over in one copy each on a copy stream, each group's verify starts when its "
-                       "copy has landed, then the logits and drafts, accept, commit and the "
-                       "device-to-host read of the target ids and accepted length; the host waits "
-                       "for each step's results" % "/".join(str(x) for x in e2e_groups),
+                       "copy has landed, then the logits and drafts, whose accept runs beside the "
+                       "verify on a second stream, commit and the device-to-host read of the target "
+                       "ids and accepted length; the host waits for each step's results"
+                       % "/".join(str(x) for x in e2e_groups),
                 "eager_value": B * T * w["L"] * e2e_k / e2e_eager_s,
                 "serial_value": B * T * w["L"] * e2e_k / e2e_serial_s,
                 "serial_how": "the same step with all inputs in one copy before the three calls"},

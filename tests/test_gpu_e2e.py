@@ -34,3 +34,21 @@ def test_pipelined_step_commits_the_same_states(groups, cuda):
         assert torch.equal(x["out"], y["out"])
     # the steps did commit (accepted length 5 >= 1), so the comparison is not of untouched states
     assert not any(torch.equal(x["state"], s0) for x, s0 in zip(single, start))
+
+
+def test_accept_beside_verify_commits_the_same_states(cuda):
+    # The timed step runs accept on a second stream beside verify (accept reads only the
+    # logits and draft ids) and commit after both; the same steps one after another on one
+    # stream give the same targets, accepted lengths, checkpoints and committed states.
+    stream = torch.cuda.Stream(device=cuda)
+    side = bench.side_stream(cuda)
+    serial = bench.make_step_sets(W, cuda, 0, 1)[0]
+    beside = bench.make_step_sets(W, cuda, 0, 1)[0]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            bench.run_step(serial, stream)
+            bench.run_step(beside, stream, side=side)
+    torch.cuda.synchronize()
+    for key in ("tgt", "acc", "out", "ckpt", "state"):
+        assert torch.equal(serial[key], beside[key]), key
+    assert int(beside["acc"][0]) == W["accept_value"]

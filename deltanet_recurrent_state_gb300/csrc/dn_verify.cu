@@ -163,7 +163,7 @@ __device__ __forceinline__ uint4 pack8_half2(const float2 *s) {
 // k/q tiles, the grams, L and M, the gate scan -- is shared by twice the rows).
 static_assert(DN_MAX_BLOCK == 16, "tile capacities 8 and 16");
 template <int DK, bool CKPT, int TM, int ROWS>
-__global__ void __launch_bounds__(256, ROWS == 64 ? 4 : (ROWS == 16 ? 6 : (TM == 8 ? 6 : 5)))
+__global__ void __launch_bounds__(256, ROWS == 64 ? (CKPT ? 4 : 5) : (ROWS == 16 ? 6 : (TM == 8 ? 6 : 5)))
 verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __half *__restrict__ k,
                  const __half *__restrict__ v, const float *__restrict__ beta,
                  const float *__restrict__ g, const __half *__restrict__ s_in,
@@ -175,10 +175,9 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     __shared__ __align__(128) uint4 sS0[ROWS * CPR];
     __shared__ __align__(128) uint4 sKQ[2 * TM * CPR];  // rows 0..TM-1 k_t, TM..2TM-1 q_t
     __shared__ float proj[ROWS][2 * TM + 1];              // [row][t] S0 k_t, [row][TM+t] S0 q_t
-    __shared__ float gram[2 * TM][TM + 1];                // [t][s] k_t.k_s, [TM+t][s] q_t.k_s
     __shared__ float sL[TM][TM], sM[TM][TM];
     __shared__ float sgam[TM], sG[TM], sbeta[TM], sg[TM];
-    __shared__ float sv[TM][ROWS], sd[TM][ROWS], so[TM][ROWS];
+    __shared__ float sv[TM][ROWS], sd[TM][ROWS];
 
     const int rblocks = DV / ROWS;
     const int rb = blockIdx.x % rblocks;
@@ -242,7 +241,9 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     }
     __syncthreads();
 
-    // 2. proj = S0 [K;Q]^T in 16x8 tiles; gram = [K;Q] K^T (one tile per warp)
+    // 2. proj = S0 [K;Q]^T in 16x8 tiles; [K;Q] K^T (one tile per warp), turned in registers
+    //    into L (strictly lower) and M (lower including the diagonal):
+    //    L[t][s] = e^{G_t - G_s} k_t.k_s (s < t), M[t][s] = e^{G_t - G_s} q_t.k_s (s <= t)
     constexpr int NG = TM / 8, MG = 2 * TM / 16;  // gram tiles: n (tokens of K), m (rows of [K;Q])
     auto proj_tile = [&](int mt, int nt) {
         float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -269,10 +270,17 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             mma_16816(e, a, b);
         }
         const int g0 = gm * 16 + (lane >> 2), h0 = gn * 8 + 2 * (lane & 3);
-        gram[g0][h0] = e[0];
-        gram[g0][h0 + 1] = e[1];
-        gram[g0 + 8][h0] = e[2];
-        gram[g0 + 8][h0 + 1] = e[3];
+        auto put = [&](int gr, int s2, float val) {  // gram row gr: k_t (gr < TM) or q_t (gr = TM + t)
+            const int t = gr < TM ? gr : gr - TM;
+            const bool keep = gr < TM ? (s2 < t) : (s2 <= t);
+            const float r = keep ? expf(sG[t] - sG[s2]) * val : 0.f;
+            if (gr < TM) sL[t][s2] = r;
+            else sM[t][s2] = r;
+        };
+        put(g0, h0, e[0]);
+        put(g0, h0 + 1, e[1]);
+        put(g0 + 8, h0, e[2]);
+        put(g0 + 8, h0 + 1, e[3]);
     };
     if constexpr (ROWS == 32) {  // warp = (m tile) * 4 + (n tile)
         if ((warp & 3) * 8 < 2 * TM) {
@@ -283,15 +291,6 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         constexpr int PN = 2 * TM / 8, PTILES = (ROWS / 16) * PN;
         for (int tile = warp; tile < PTILES; tile += NT / 32) proj_tile(tile / PN, tile % PN);
         if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
-    }
-    __syncthreads();
-
-    // 3. L (strictly lower) and M (lower incl. diagonal), one entry per thread
-    if (tid < TM * TM) {
-        const int t = tid / TM, s2 = tid % TM;
-        const float r = (s2 <= t) ? expf(sG[t] - sG[s2]) : 0.f;
-        sL[t][s2] = (s2 < t) ? r * gram[t][s2] : 0.f;
-        sM[t][s2] = r * gram[TM + t][s2];
     }
     __syncthreads();
 
@@ -337,17 +336,12 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         dst += tstride;
     }
 
-    // 6. outputs
+    // 6. outputs, stored straight from registers (consecutive threads, consecutive rows)
     for (int i = tid; i < T * ROWS; i += NT) {
         const int t = i / ROWS, r = i % ROWS;
         float o = sgam[t] * proj[r][TM + t];
         for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
-        so[t][r] = o;
-    }
-    __syncthreads();
-    for (int i = tid; i < T * ROWS; i += NT) {
-        const int t = i / ROWS, r = i % ROWS;
-        out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(so[t][r]);
+        out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(o);
     }
 }
 

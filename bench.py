@@ -260,9 +260,10 @@ def run_step(x, stream, evs=None, side=None):
         evs[3].record(stream)
 
 
-def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True):
+def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True, by_set=None):
     """Warm up, then time exactly `steps` steps between barriers; returns (seconds,
-    per-kernel mean ms [verify, accept, commit], wall-clock bounds). Accept runs on a second
+    per-kernel mean ms [verify, accept, commit], wall-clock bounds). With a list `by_set`,
+    it also receives (set index, [verify, accept, commit] ms) of every eager step. Accept runs on a second
     stream beside verify (run_step). With `graphs`, each buffer set's step (the three calls)
     is captured once in a CUDA graph and a timed step is one replay, as a serving loop
     launches a fixed step; the per-kernel durations then come from a separate eager pass with
@@ -314,6 +315,8 @@ def timed_steps(sets, steps, warmup, stream, dist, per_kernel=True, graphs=True)
                 run_step(sets[i % len(sets)], stream, evs[i])
         torch.cuda.synchronize()
         per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(3)]
+        if by_set is not None:
+            by_set.extend((i % len(sets), [e[j].elapsed_time(e[j + 1]) for j in range(3)]) for i, e in enumerate(evs))
     return secs, per, (t_wall0, t_wall1)
 
 
@@ -710,11 +713,15 @@ def decode_row(device, stream, steps=1000, warmup=10, nsets=8):
     from deltanet_recurrent_state_gb300.workloads import WORKLOADS
     w = WORKLOADS["decode_loop_l48_h48_d128_t8_f16"]
     sets = make_step_sets(w, device, 0, nsets)
-    secs, per, _ = timed_steps(sets, steps, warmup, stream, None)
+    by_set = []
+    secs, per, _ = timed_steps(sets, steps, warmup, stream, None, by_set=by_set)
     N, B, T = w["L"] * w["B"], w["B"], w["T"]
     vb = verify_bytes(N, T, w["H"], w["dk"], w["dv"], 2)
     plans = [int(x["acc_plan"][0]) for x in sets]
-    cb = statistics.mean(commit_bytes(w["L"], x["acc_plan"], w["H"], w["dk"], w["dv"], 2) for x in sets)
+    cbs = [commit_bytes(w["L"], x["acc_plan"], w["H"], w["dk"], w["dv"], 2) for x in sets]
+    cb = statistics.mean(cbs)
+    # the steps whose request accepted at least one token (the others launch commit but copy nothing)
+    copying = [(cbs[i], ms[2]) for i, ms in by_set if cbs[i] > 0]
     res = {"workload": "decode_loop_l48_h48_d128_t8_f16", "steps": steps,
            "ms_per_step": secs / steps * 1e3, "loop_ms": secs * 1e3,
            "token_layers_per_s": B * T * w["L"] * steps / secs,
@@ -722,6 +729,10 @@ def decode_row(device, stream, steps=1000, warmup=10, nsets=8):
            "verify_ms": per[0], "verify_gbs": vb / (per[0] / 1e3) / 1e9,
            "accept_ms": per[1], "commit_ms": per[2],
            "commit_gbs": cb / (per[2] / 1e3) / 1e9 if per[2] > 0 else None}
+    if copying:
+        ms_copy = statistics.mean(t for _, t in copying)
+        res["commit_copying_steps"] = {"steps": len(copying), "ms": ms_copy,
+                                       "gbs": statistics.mean(b for b, _ in copying) / (ms_copy / 1e3) / 1e9}
     del sets
     return res
 

@@ -87,7 +87,7 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
     constexpr int ROWS = kDeltaRows, CPR = DK / 8, NTW = DK / 16;  // 16-byte chunks per row; n-tiles per warp
     __shared__ __align__(16) uint4 sS[ROWS * CPR];                  // the state rows, fp16
     __shared__ __align__(16) __half sK[DN_MAX_BLOCK][DK + 8];       // the accepted keys (zeros past a)
-    __shared__ float sD[DN_MAX_BLOCK][ROWS + 8];                    // D[s][row] (zeros past a)
+    __shared__ __align__(16) float sD[DN_MAX_BLOCK][ROWS + 8];     // delta_s[row] (zeros past a)
     __shared__ float sgate[DN_MAX_BLOCK + 1];  // decay of each position, then Gam
     const int rblocks = DV / ROWS;
     const int rb = blockIdx.x % rblocks;
@@ -101,9 +101,8 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
     const int gid = lane >> 2, t4 = lane & 3;
     uint4 *sp = reinterpret_cast<uint4 *>(state + ((n * H + h) * (size_t)DV + rb * ROWS) * DK);
 
-    // The state rows (chunk c of row r at c ^ (r & 7)) and the keys (zeros past a) go in by
-    // cp.async first; they are not needed before the MMA (keys) and the epilogue (rows), so
-    // their latency overlaps the gates and D below.
+    // The state rows (chunk c of row r at c ^ (r & 7)), the keys and the deltas (zeros past a)
+    // go in by cp.async first, all in flight together; their latency overlaps the gates below.
     for (int i = tid; i < ROWS * CPR; i += 256) {
         const int r = i / CPR, c = i % CPR;
         cp_async16(&sS[r * CPR + (c ^ (r & 7))], sp + i, 16);
@@ -112,6 +111,13 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
         const int s2 = i / (DK / 8), j8 = i % (DK / 8);
         const bool live = s2 < a;
         cp_async16(&sK[s2][8 * j8], live ? (const void *)(k + ((n * T + s2) * H + h) * DK + (size_t)j8 * 8) : (const void *)k,
+                   live ? 16 : 0);
+    }
+    for (int i = tid; i < DN_MAX_BLOCK * (ROWS / 4); i += 256) {
+        const int s2 = i / (ROWS / 4), j4 = i % (ROWS / 4);
+        const bool live = s2 < a;
+        cp_async16(&sD[s2][4 * j4],
+                   live ? (const void *)(delta + ((n * T + s2) * H + h) * DV + rb * ROWS + 4 * j4) : (const void *)delta,
                    live ? 16 : 0);
     }
     cp_async_commit();
@@ -128,12 +134,6 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
         if (lane < DN_MAX_BLOCK) sgate[lane] = lane + 1 < 32 ? excl : 1.f;
         if (lane == 0) sgate[DN_MAX_BLOCK] = suf;  // the product of every gate: Gam
     }
-    __syncthreads();
-    // D[s][row] = decay_s delta_s[row], zeros past a
-    for (int i = tid; i < DN_MAX_BLOCK * ROWS; i += 256) {
-        const int s2 = i / ROWS, r = i % ROWS;
-        sD[s2][r] = s2 < a ? sgate[s2] * __ldg(&delta[((n * T + s2) * H + h) * DV + rb * ROWS + r]) : 0.f;
-    }
     cp_async_wait<0>();
     __syncthreads();
     const float gam = sgate[DN_MAX_BLOCK];
@@ -149,8 +149,10 @@ commit_deltas_kernel(int B, int H, int T, int DV, const __half *__restrict__ k,
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             if (8 * ks >= a) break;
-            const float x[4] = {sD[8 * ks + t4][m0 + gid], sD[8 * ks + t4][m0 + gid + 8],
-                                sD[8 * ks + t4 + 4][m0 + gid], sD[8 * ks + t4 + 4][m0 + gid + 8]};
+            // D[s][row] = decay_s delta_s[row]
+            const float d0 = sgate[8 * ks + t4], d1 = sgate[8 * ks + t4 + 4];
+            const float x[4] = {d0 * sD[8 * ks + t4][m0 + gid], d0 * sD[8 * ks + t4][m0 + gid + 8],
+                                d1 * sD[8 * ks + t4 + 4][m0 + gid], d1 * sD[8 * ks + t4 + 4][m0 + gid + 8]};
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -200,7 +202,7 @@ extern "C" dn_status dn_commit_deltas(int N, int B, int H, int T, int dk, int dv
     if (state_dt != DN_F16) return DN_ERR_UNSUPPORTED;
     if (N == 0) return DN_OK;
     if (!k || !g || !delta || !accepted_len || !state) return DN_ERR_INVALID_ARG;
-    if (!aligned(k, 16) || !aligned(state, 16) || !aligned(delta, 4) || !aligned(g, 4) ||
+    if (!aligned(k, 16) || !aligned(state, 16) || !aligned(delta, 16) || !aligned(g, 4) ||
         !aligned(accepted_len, 4))
         return DN_ERR_INVALID_ARG;
     if ((long long)N * H * (dv / kDeltaRows) > 0x7fffffffLL) return DN_ERR_INVALID_ARG;

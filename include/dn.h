@@ -144,7 +144,7 @@ dn_status dn_verify_block(int N, int H, int T, int dk, int dv,
  * dn_commit_deltas: N, B, H, T, dk, dv, state_dt and accepted_len as dn_commit, with
  *   k        [N][T][H][dk] the block's keys (io dtype), 16-byte aligned
  *   g        [N][T][H] fp32 the block's gates
- *   delta    [N][T][H][dv] fp32 from dn_verify_block_deltas
+ *   delta    [N][T][H][dv] fp32 from dn_verify_block_deltas, 16-byte aligned
  *   state    [N][H][dv][dk], updated in place (must be dn_verify_block_deltas' state_in)
  * Both support the fp16 state / fp16 io pair only (DN_ERR_UNSUPPORTED otherwise).
  */

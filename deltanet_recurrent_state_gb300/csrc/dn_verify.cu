@@ -177,7 +177,8 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     __shared__ float proj[ROWS][2 * TM + 1];              // [row][t] S0 k_t, [row][TM+t] S0 q_t
     __shared__ float sL[TM][TM], sM[TM][TM];
     __shared__ float sgam[TM], sG[TM], sbeta[TM], sg[TM];
-    __shared__ float sv[TM][ROWS], sd[TM][ROWS];
+    __shared__ __align__(16) __half sv[TM][ROWS];
+    __shared__ float sd[TM][ROWS];
 
     const int rblocks = DV / ROWS;
     const int rb = blockIdx.x % rblocks;
@@ -190,35 +191,29 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
     grid_dep_wait();
     grid_dep_trigger();
 
-    // 1. state chunks c*TPR + ln of this lane's row: fp16 to shared, fp32 to registers
-    float2 s[NCH * 4];
+    // 1. The state rows, k_t and q_t (zeros past T) and the rows' v_t go to shared memory by
+    //    cp.async, all in flight at once (one memory latency for the prologue); the gates load
+    //    meanwhile. After the barrier each lane takes its state chunks to fp32 registers.
     {
         const __half *sp = s_in + (n * H + h) * set_elems + (size_t)row * DK;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
             const int j = c * TPR + ln;
-            const uint4 u = *reinterpret_cast<const uint4 *>(sp + j * 8);
-            sS0[hsw<CPR>(lr, j)] = u;
-            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
+            cp_async16(&sS0[hsw<CPR>(lr, j)], sp + j * 8, 16);
         }
     }
     for (int i = tid; i < TM * CPR; i += NT) {
         const int t = i / CPR, j = i % CPR;
-        uint4 uk = make_uint4(0u, 0u, 0u, 0u), uq = uk;  // rows past T stay zero
-        if (t < T) {
-            const size_t off = ((n * T + t) * H + h) * DK + (size_t)j * 8;
-            uk = *reinterpret_cast<const uint4 *>(k + off);
-            uq = *reinterpret_cast<const uint4 *>(q + off);
-        }
-        sKQ[hsw<CPR>(t, j)] = uk;
-        sKQ[hsw<CPR>(TM + t, j)] = uq;
+        const bool live = t < T;
+        const size_t off = live ? ((n * T + t) * H + h) * DK + (size_t)j * 8 : 0;
+        cp_async16(&sKQ[hsw<CPR>(t, j)], k + off, live ? 16 : 0);
+        cp_async16(&sKQ[hsw<CPR>(TM + t, j)], q + off, live ? 16 : 0);
     }
-    for (int i = tid; i < T * ROWS; i += NT) {
-        const int t = i / ROWS, r = i % ROWS;
-        sv[t][r] = __half2float(v[((n * T + t) * H + h) * DV + rb * ROWS + r]);
+    for (int i = tid; i < T * (ROWS / 8); i += NT) {
+        const int t = i / (ROWS / 8), j = i % (ROWS / 8);
+        cp_async16(&sv[t][8 * j], v + ((n * T + t) * H + h) * DV + rb * ROWS + 8 * j, 16);
     }
+    cp_async_commit();
     if (warp == 0) {
         // G_t = sum_{r<=t} log g_r: inclusive scan over lanes 0..15
         float lg = 0.f, gg = 1.f, bb = 0.f;
@@ -239,7 +234,16 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
             sbeta[lane] = bb;
         }
     }
+    cp_async_wait<0>();
     __syncthreads();
+    float2 s[NCH * 4];  // this lane's state chunks c*TPR + ln, fp32
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+        const uint4 u = sS0[hsw<CPR>(lr, c * TPR + ln)];
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
+    }
 
     // 2. proj = S0 [K;Q]^T in 16x8 tiles; [K;Q] K^T (one tile per warp), turned in registers
     //    into L (strictly lower) and M (lower including the diagonal):
@@ -305,7 +309,7 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
                 float acc = 0.f;
 #pragma unroll
                 for (int s2 = 0; s2 < t; ++s2) acc = fmaf(sL[t][s2], dl[s2], acc);
-                dl[t] = sbeta[t] * (sv[t][rl] - sgam[t] * proj[rl][t] - acc);
+                dl[t] = sbeta[t] * (__half2float(sv[t][rl]) - sgam[t] * proj[rl][t] - acc);
                 sd[t][rl] = dl[t];
             }
         }

@@ -245,35 +245,19 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         for (int i = 0; i < 4; ++i) s[c * 4 + i] = __half22float2(h2[i]);
     }
 
-    // 2. proj = S0 [K;Q]^T in 16x8 tiles; [K;Q] K^T (one tile per warp), turned in registers
-    //    into L (strictly lower) and M (lower including the diagonal):
+    // 2. proj = S0 [K;Q]^T in 16x8 tiles; [K;Q] K^T, turned in registers into L (strictly
+    //    lower) and M (lower including the diagonal):
     //    L[t][s] = e^{G_t - G_s} k_t.k_s (s < t), M[t][s] = e^{G_t - G_s} q_t.k_s (s <= t)
     constexpr int NG = TM / 8, MG = 2 * TM / 16;  // gram tiles: n (tokens of K), m (rows of [K;Q])
-    auto proj_tile = [&](int mt, int nt) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            unsigned a[4], b[2];
-            ldsm_x4(a, &sS0[hsw<CPR>(mt * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
-            ldsm_x2(b, &sKQ[hsw<CPR>(nt * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
-            mma_16816(d, a, b);
-        }
-        const int r0 = mt * 16 + (lane >> 2), c0 = nt * 8 + 2 * (lane & 3);
+    auto proj_epi = [&](int m, int nn, const float (&d)[4]) {
+        const int r0 = m * 16 + (lane >> 2), c0 = nn * 8 + 2 * (lane & 3);
         proj[r0][c0] = d[0];
         proj[r0][c0 + 1] = d[1];
         proj[r0 + 8][c0] = d[2];
         proj[r0 + 8][c0 + 1] = d[3];
     };
-    auto gram_tile = [&](int gm, int gn) {
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            unsigned a[4], b[2];
-            ldsm_x4(a, &sKQ[hsw<CPR>(gm * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
-            ldsm_x2(b, &sKQ[hsw<CPR>(gn * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
-            mma_16816(e, a, b);
-        }
-        const int g0 = gm * 16 + (lane >> 2), h0 = gn * 8 + 2 * (lane & 3);
+    auto gram_epi = [&](int m, int nn, const float (&e)[4]) {
+        const int g0 = m * 16 + (lane >> 2), h0 = nn * 8 + 2 * (lane & 3);
         auto put = [&](int gr, int s2, float val) {  // gram row gr: k_t (gr < TM) or q_t (gr = TM + t)
             const int t = gr < TM ? gr : gr - TM;
             const bool keep = gr < TM ? (s2 < t) : (s2 <= t);
@@ -286,15 +270,70 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         put(g0 + 8, h0, e[2]);
         put(g0 + 8, h0 + 1, e[3]);
     };
-    if constexpr (ROWS == 32) {  // warp = (m tile) * 4 + (n tile)
-        if ((warp & 3) * 8 < 2 * TM) {
-            proj_tile(warp >> 2, warp & 3);
+    auto proj_tile = [&](int mt, int nt) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            unsigned a[4], b[2];
+            ldsm_x4(a, &sS0[hsw<CPR>(mt * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+            ldsm_x2(b, &sKQ[hsw<CPR>(nt * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+            mma_16816(d, a, b);
+        }
+        proj_epi(mt, nt, d);
+    };
+    auto gram_tile = [&](int gm, int gn) {
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            unsigned a[4], b[2];
+            ldsm_x4(a, &sKQ[hsw<CPR>(gm * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+            ldsm_x2(b, &sKQ[hsw<CPR>(gn * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+            mma_16816(e, a, b);
+        }
+        gram_epi(gm, gn, e);
+    };
+    if constexpr (ROWS == 64) {
+        constexpr int PN = 2 * TM / 8, PTILES = (ROWS / 16) * PN, GTILES = MG * NG, NWARP = NT / 32;
+        // 64-row CTAs: every warp holds PPW projection tiles (warp, warp + 8) and warps 7, 6, ..
+        // a gram tile too; the tiles' k-loops run side by side, each with its own accumulator,
+        // in the same order as one tile alone.
+        constexpr int PPW = PTILES / NWARP;
+        static_assert(PTILES % NWARP == 0 && PPW <= 2 && GTILES <= NWARP, "tiles per warp");
+        const bool hasg = NWARP - 1 - warp < GTILES;
+        const int q2 = NWARP - 1 - warp;
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        const int m0 = warp / PN, n0 = warp % PN, m1 = (warp + NWARP) / PN, n1 = (warp + NWARP) % PN;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            unsigned a[4], b[2];
+            ldsm_x4(a, &sS0[hsw<CPR>(m0 * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+            ldsm_x2(b, &sKQ[hsw<CPR>(n0 * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+            mma_16816(d0, a, b);
+            if constexpr (PPW == 2) {
+                ldsm_x4(a, &sS0[hsw<CPR>(m1 * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+                ldsm_x2(b, &sKQ[hsw<CPR>(n1 * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+                mma_16816(d1, a, b);
+            }
+            if (hasg) {
+                ldsm_x4(a, &sKQ[hsw<CPR>((q2 / NG) * 16 + (lane & 15), 2 * ks + (lane >> 4))]);
+                ldsm_x2(b, &sKQ[hsw<CPR>((q2 % NG) * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1))]);
+                mma_16816(e, a, b);
+            }
+        }
+        proj_epi(m0, n0, d0);
+        if constexpr (PPW == 2) proj_epi(m1, n1, d1);
+        if (hasg) gram_epi(q2 / NG, q2 % NG, e);
+    } else {
+        if constexpr (ROWS == 32) {  // warp = (m tile) * 4 + (n tile)
+            if ((warp & 3) * 8 < 2 * TM) {
+                proj_tile(warp >> 2, warp & 3);
+                if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
+            }
+        } else {
+            constexpr int PN = 2 * TM / 8, PTILES = (ROWS / 16) * PN;
+            for (int tile = warp; tile < PTILES; tile += NT / 32) proj_tile(tile / PN, tile % PN);
             if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
         }
-    } else {
-        constexpr int PN = 2 * TM / 8, PTILES = (ROWS / 16) * PN;
-        for (int tile = warp; tile < PTILES; tile += NT / 32) proj_tile(tile / PN, tile % PN);
-        if (warp < MG * NG) gram_tile(warp / NG, warp % NG);
     }
     __syncthreads();
 
@@ -340,12 +379,27 @@ verify_wy_kernel(int H, int T, int DV, const __half *__restrict__ q, const __hal
         dst += tstride;
     }
 
-    // 6. outputs, stored straight from registers (consecutive threads, consecutive rows)
-    for (int i = tid; i < T * ROWS; i += NT) {
-        const int t = i / ROWS, r = i % ROWS;
-        float o = sgam[t] * proj[r][TM + t];
-        for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
-        out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(o);
+    // 6. outputs, stored straight from registers (consecutive threads, consecutive rows). In
+    //    64-row CTAs a thread's four outputs are unrolled so that their sums run side by side.
+    if constexpr (ROWS == 64) {
+        constexpr int KO = (TM * ROWS + NT - 1) / NT;
+#pragma unroll
+        for (int k2 = 0; k2 < KO; ++k2) {
+            const int i = tid + k2 * NT;
+            if (i < T * ROWS) {
+                const int t = i / ROWS, r = i % ROWS;
+                float o = sgam[t] * proj[r][TM + t];
+                for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
+                out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(o);
+            }
+        }
+    } else {
+        for (int i = tid; i < T * ROWS; i += NT) {
+            const int t = i / ROWS, r = i % ROWS;
+            float o = sgam[t] * proj[r][TM + t];
+            for (int s2 = 0; s2 <= t; ++s2) o = fmaf(sM[t][s2], sd[s2][r], o);
+            out[((n * T + t) * H + h) * DV + rb * ROWS + r] = __float2half_rn(o);
+        }
     }
 }
 

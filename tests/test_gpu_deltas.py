@@ -41,6 +41,23 @@ def _assert_within_one_ulp(got, want):
     assert (got == want).float().mean().item() > 0.99
 
 
+@pytest.mark.parametrize("a", [0, 1, 5, 16])
+def test_beta0_g1_deltas_commit_keeps_the_state(a, cuda):
+    # beta = 0, g = 1: every delta is zero and every decay one, so the committed state is the
+    # initial state bit for bit whatever the accepted length
+    N, T, H, d = 3, 16, 4, 128
+    x = inputs.recurrence_inputs(N, T, H, d, d, seed=19, device=cuda)
+    x["beta"].zero_()
+    x["g"].fill_(1.0)
+    _, delta = dn.dn_verify_block_deltas(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    s_d = x["state"].clone()
+    acc = torch.full((1,), a, dtype=torch.int32, device=cuda)
+    dn.dn_commit_deltas(x["k"], x["g"], delta, acc, s_d)
+    torch.cuda.synchronize()
+    assert torch.equal(delta, torch.zeros_like(delta))
+    assert torch.equal(s_d, x["state"])
+
+
 @pytest.mark.parametrize("a_all", [1, 8, 9, 16])
 def test_deltas_commit_full_size_against_checkpoint_path(a_all, cuda):
     # the single-user launch shape (48 layers x 48 heads x 128 x 128), every set at one length

@@ -56,6 +56,23 @@ def test_fp16_chunkwise_edges(P, dk, dv, cuda):
     assert_close("state_out", s_out, ref[2], TOL["f16"])
 
 
+@pytest.mark.parametrize("engine", ["mma", "tc"])
+def test_beta0_g1_prefill_keeps_the_state(engine, cuda):
+    # beta = 0, g = 1: nothing is written, so every checkpoint and the final state are the initial
+    # state bit for bit, and each output is S0 q_t
+    N, P, H, d = 2, 200, 3, 128
+    x = inputs.recurrence_inputs(N, P, H, d, d, seed=18, device=cuda)
+    x["beta"].zero_()
+    x["g"].fill_(1.0)
+    out, ckpt, s_out = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"], engine=engine)
+    torch.cuda.synchronize()
+    assert torch.equal(s_out, x["state"])
+    for c in range(P // 64):
+        assert torch.equal(ckpt[:, c], x["state"])
+    want = np.einsum("nhij,nphj->nphi", np64(x["state"]), np64(x["q"]))
+    assert_close("out = S0 q", out, want, TOL["f16"])
+
+
 def test_restore_from_checkpoint_is_bit_identical(cuda):
     N, P, H, d = 1, 300, 4, 128
     x = inputs.recurrence_inputs(N, P, H, d, d, seed=301, device=cuda)

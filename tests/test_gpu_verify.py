@@ -75,6 +75,29 @@ def test_beta0_g1_leaves_state_unchanged_on_gpu(cuda):
         assert torch.equal(ckpt[:, t], x["state"])
 
 
+@pytest.mark.parametrize("dt", ["f16", "f32"])
+def test_unit_key_write_identity_on_gpu(dt, cuda):
+    # beta = 1, g = 1: S_t k_t = (1 - |k_t|^2) S_{t-1} k_t + |k_t|^2 v_t, so S_t k_t = v_t for a
+    # unit key (the delta rule writes v_t under k_t). Checked from the stored checkpoints in
+    # float64, independent of the oracle; the residual is the checkpoints' own rounding.
+    N, T, H, d = 2, 8, 3, 128
+    x = inputs.recurrence_inputs(N, T, H, d, d, io=dt, state=dt, seed=17, device=cuda)
+    x["beta"].fill_(1.0)
+    x["g"].fill_(1.0)
+    _, ckpt = dn.dn_verify_block(x["q"], x["k"], x["v"], x["beta"], x["g"], x["state"])
+    torch.cuda.synchronize()
+    k, v = np64(x["k"]), np64(x["v"])
+    prev = np64(x["state"])
+    for t in range(T):
+        st = np64(ckpt[:, t])
+        kt, vt = k[:, t], v[:, t]                      # [N, H, d]
+        kk = (kt * kt).sum(-1, keepdims=True)
+        want = (1.0 - kk) * np.einsum("nhij,nhj->nhi", prev, kt) + kk * vt
+        got = np.einsum("nhij,nhj->nhi", st, kt)
+        assert_close("S_t k_t", got, want, TOL[dt])
+        prev = st
+
+
 def test_outputs_do_not_spill_past_their_buffers(cuda):
     # canaries after out and ckpt stay untouched
     N, T, H, d = 2, 5, 3, 64

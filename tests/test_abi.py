@@ -148,6 +148,28 @@ def test_commit_rejects(lib, over, want):
     assert lib.dn_commit(*_commit_args(buf, **over)) == want
 
 
+def _commit_deltas_args(buf, **over):
+    a = dict(N=2, B=1, H=1, T=2, dk=64, dv=64, st=F16, k=buf(2 * 2 * 64 * 2), g=buf(),
+             delta=buf(2 * 2 * 64 * 4), acc=buf(), s=buf(2 * 64 * 64 * 2))
+    a.update(over)
+    return (a["N"], a["B"], a["H"], a["T"], a["dk"], a["dv"], a["st"], a["k"], a["g"], a["delta"], a["acc"],
+            a["s"], None)
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(B=0), INVALID), (dict(N=3, B=2), INVALID), (dict(T=17), INVALID), (dict(st=F32), UNSUPPORTED),
+    (dict(dk=100), UNSUPPORTED), (dict(delta=None), INVALID), (dict(k=None), INVALID),
+    ("misaligned_delta", INVALID), ("misaligned_state", INVALID),
+])
+def test_commit_deltas_rejects(lib, over, want):
+    buf = Bufs()
+    if over == "misaligned_delta":  # the deltas go in by 16-byte copies
+        over = dict(delta=buf(offset=4))
+    elif over == "misaligned_state":
+        over = dict(s=buf(offset=8))
+    assert lib.dn_commit_deltas(*_commit_deltas_args(buf, **over)) == want
+
+
 def _prefill_args(buf, **over):
     a = dict(N=1, H=1, P=70, chunk=64, dk=64, dv=64, io=F32, st=F32, q=buf(70 * 256),
              k=buf(70 * 256), v=buf(70 * 256), beta=buf(), g=buf(), s_in=None, out=buf(70 * 256),

@@ -334,6 +334,15 @@ def e2e_group_bounds(L, groups):
     return [sum(sizes[:i]) for i in range(len(sizes) + 1)]
 
 
+def e2e_growing_groups(L):
+    """Group sizes of the pipelined end-to-end step: L/12, L/6, L/3 and the rest (4, 8, 16, 20
+    for 48 layers), or one group when L is too small to split."""
+    if L < 12:
+        return [L]
+    sizes = [L // 12, L // 6, L // 3]
+    return sizes + [L - sum(sizes)]
+
+
 def e2e_steps(w, sets, steps, warmup, stream, device, graphs=True, groups=1):
     """The same step through the public API with host inputs: every step copies its
     inputs from pinned host memory and reads its results back (the target ids and the
@@ -929,11 +938,10 @@ def main():
     value = units_per_rank * world / secs
 
     e2e_k = max(3, min(args.steps, 200))
-    # layer groups of the pipelined step, growing (48 layers: 8, 16, 24): the first group's
-    # copy is short so the verify starts early, and each later copy lands before the verify
-    # of the groups before it ends (copies move a layer in ~3.4 us, verify takes ~4.3 us)
-    L6 = w["L"] // 6
-    e2e_groups = (L6, 2 * L6, w["L"] - 3 * L6)
+    # layer groups of the pipelined step, growing (48 layers: 4, 8, 16, 20): the first group's
+    # copy is short so the verify starts early, and each later copy lands about when the
+    # verify of the groups before it ends (copies move a layer in ~3.4 us, verify takes ~4.3 us)
+    e2e_groups = e2e_growing_groups(w["L"])
     e2e_s, h2d, d2h = e2e_steps(w, sets, e2e_k, 3, stream, device, groups=e2e_groups)
     e2e_value = B * T * w["L"] * e2e_k / e2e_s
     e2e_eager_s, _, _ = e2e_steps(w, sets, e2e_k, 3, stream, device, graphs=False, groups=e2e_groups)

@@ -109,3 +109,11 @@ def test_e2e_group_bounds():
     for bad in (5, 0, (8, 16), (8, 16, 25), (0, 24, 24)):
         with pytest.raises(ValueError):
             bench.e2e_group_bounds(48, bad)
+
+
+def test_e2e_growing_groups_cover_the_layers():
+    assert bench.e2e_growing_groups(48) == [4, 8, 16, 20]
+    for L in (1, 5, 11, 12, 13, 47, 48, 96):
+        g = bench.e2e_growing_groups(L)
+        assert sum(g) == L and min(g) >= 1
+        assert bench.e2e_group_bounds(L, g)[-1] == L

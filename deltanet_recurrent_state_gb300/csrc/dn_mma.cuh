@@ -76,18 +76,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *mb, un
     const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(a), "r"(bytes) : "memory");
 }
-// Bounded wait for the phase with the given parity; false if it did not complete within
-// `tries` polls (the caller reports it instead of hanging).
-__device__ __forceinline__ bool mbar_wait(unsigned long long *mb, unsigned parity, int tries) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(mb);
-    for (int it = 0; it < tries; ++it) {
-        unsigned ok;
-        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-                     " selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(a), "r"(parity) : "memory");
-        if (ok) return true;
-    }
-    return false;
-}
 __device__ __forceinline__ unsigned long long global_timer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

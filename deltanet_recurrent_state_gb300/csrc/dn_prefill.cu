@@ -167,6 +167,16 @@ prefill_seq_kernel(int H, int P, int DV, int chunk, const IO *__restrict__ q,
 // Shared-memory tiles. q/k/v, O and the checkpoint move with the tensor-map (TMA) engine
 // in 64-column boxes of 128-byte rows, swizzled by the engine: 16-byte chunk c of row r
 // of a box sits at chunk c ^ (r & 7). Every box starts on a 1024-byte boundary.
+// A = beta_t e^{G_t - G_s} k_t.k_s of sub-chunk j, 16 x 16 fp32: element (i, s) at
+// j kAStride + 16 i + 4 ((s >> 2) ^ ((i >> 1) & 3)) + (s & 3). Each row is four 16-byte groups,
+// so the inverse reads a row four elements at a time; the groups are swizzled by row so that
+// the grams' pair stores spread over the banks, and sub-chunks sit 260 floats apart so that
+// one warp's reads of two sub-chunks hit different banks.
+constexpr int kAStride = 260;
+__device__ __forceinline__ int a_index(int j, int i, int s) {
+    return j * kAStride + 16 * i + 4 * ((s >> 2) ^ ((i >> 1) & 3)) + (s & 3);
+}
+
 template <int DK, int DVC>
 struct PrefillSmem {
     static constexpr int C = 64, NSUB = 4, NKQV = 3, NPREP = 2;
@@ -182,8 +192,8 @@ struct PrefillSmem {
     static constexpr size_t kMq = kTb + NPREP * NSUB * 16 * 24 * 2;      // [2][NSUB][16][24] half
     static constexpr size_t kGam = kMq + NPREP * NSUB * 16 * 24 * 2;     // [2][C] float
     static constexpr size_t kDec = kGam + NPREP * C * 4;                 // [2][C] float
-    static constexpr size_t kA = kDec + NPREP * C * 4;                   // [NSUB][16][17] float
-    static constexpr size_t kGates = kA + NSUB * 16 * 17 * 4;            // [3][2][C] float: beta, g
+    static constexpr size_t kA = kDec + NPREP * C * 4;                   // [NSUB][kAStride] float
+    static constexpr size_t kGates = kA + NSUB * kAStride * 4;           // [3][2][C] float: beta, g
     static constexpr size_t kMbar = kGates + (size_t)NKQV * 2 * C * 4;   // [3] mbarrier
     static constexpr size_t kAbort = kMbar + NKQV * 8;                   // int: a wait ran out
     static constexpr size_t kBytes = kAbort + 8;
@@ -282,7 +292,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
     __half(*sMq)[NSUB][16][24] = reinterpret_cast<__half(*)[NSUB][16][24]>(smem + L::kMq);
     float(*sgam)[C] = reinterpret_cast<float(*)[C]>(smem + L::kGam);
     float(*sdec)[C] = reinterpret_cast<float(*)[C]>(smem + L::kDec);
-    float(*sA)[16][17] = reinterpret_cast<float(*)[16][17]>(smem + L::kA);
+    float *sA = reinterpret_cast<float *>(smem + L::kA);
     float(*sGates)[2][C] = reinterpret_cast<float(*)[2][C]>(smem + L::kGates);  // [buf][beta|g][t]
     unsigned long long *mbar = reinterpret_cast<unsigned long long *>(smem + L::kMbar);
     // Raised when a wait runs out (kWaitBudgetNs): from then on no role issues copies or global
@@ -446,11 +456,17 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 const float v1[4] = {e0[2], e0[3], e1[2], e1[3]};  // row fr + 8
                 if (!isq) {
                     const float b0r = sbeta[16 * j + fr], b1r = sbeta[16 * j + fr + 8];
+                    float a0[4], a1[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        sA[j][fr][cs[w]] = (cs[w] < fr) ? b0r * __expf(Gr0 - Gc[w]) * v0[w] : 0.f;
-                        sA[j][fr + 8][cs[w]] = (cs[w] < fr + 8) ? b1r * __expf(Gr1 - Gc[w]) * v1[w] : 0.f;
+                        a0[w] = (cs[w] < fr) ? b0r * __expf(Gr0 - Gc[w]) * v0[w] : 0.f;
+                        a1[w] = (cs[w] < fr + 8) ? b1r * __expf(Gr1 - Gc[w]) * v1[w] : 0.f;
                     }
+                    // columns (fc, fc + 1) and (fc + 8, fc + 9) are pairs within a 16-byte group
+                    *reinterpret_cast<float2 *>(sA + a_index(j, fr, fc)) = make_float2(a0[0], a0[1]);
+                    *reinterpret_cast<float2 *>(sA + a_index(j, fr, fc + 8)) = make_float2(a0[2], a0[3]);
+                    *reinterpret_cast<float2 *>(sA + a_index(j, fr + 8, fc)) = make_float2(a1[0], a1[1]);
+                    *reinterpret_cast<float2 *>(sA + a_index(j, fr + 8, fc + 8)) = make_float2(a1[2], a1[3]);
                 } else {
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
@@ -462,7 +478,7 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
             }
             bar_sync(kBarPrep, NTP);
             // Tb = (I + A)^{-1} diag(beta): one thread per (sub-chunk, column), forward
-            // substitution in fp32
+            // substitution in fp32; row i of A is read four elements at a time
             if (pt < NSUB * 16) {
                 const int j = pt >> 4, col = pt & 15;
                 float x[16];
@@ -470,7 +486,13 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                 for (int i = 0; i < 16; ++i) {
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int kk = 0; kk < i; ++kk) acc[kk & 3] = fmaf(sA[j][i][kk], x[kk], acc[kk & 3]);
+                    for (int g4 = 0; g4 < (i + 3) / 4; ++g4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(sA + a_index(j, i, 4 * g4));
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (4 * g4 + u < i) acc[u] = fmaf(av[u], x[4 * g4 + u], acc[u]);
+                    }
                     x[i] = (i < col) ? 0.f : (i == col ? 1.f : -((acc[0] + acc[1]) + (acc[2] + acc[3])));
                 }
                 const float bc = sbeta[16 * j + col];

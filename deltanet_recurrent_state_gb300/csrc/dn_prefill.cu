@@ -410,30 +410,39 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
             // grams by MMA, tile = (sub-chunk j, K or Q rows) x K_j^T, with the gate scan of
             // the sub-chunk in the same warp; the epilogue applies the decays in registers:
             // A = beta_t e^{G_t-G_s} k_t.k_s (s < t), Mq = e^{G_t-G_s} q_t.k_s (s <= t).
-            // A warp's tiles run their k-loops side by side (independent accumulators).
+            // A warp's tiles run their k-loops side by side (independent accumulators). With
+            // two tiles a warp, warp pw takes sub-chunk pw's K and Q tiles, which share the
+            // K_j fragments (three fragment loads a k-step instead of four).
             constexpr int TPW = 2 * NSUB / (NTP / 32);  // gram tiles per prep warp
+            auto tile_of = [&](int u) { return TPW == 2 ? 2 * pw + u : pw + u * (NTP / 32); };
             float e[TPW][2][4];
 #pragma unroll
             for (int u = 0; u < TPW; ++u)
 #pragma unroll
                 for (int w = 0; w < 4; ++w) e[u][0][w] = e[u][1][w] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
+            for (int ks = 0; ks < KS; ++ks) {
+                unsigned bb[4];
+                if constexpr (TPW == 2)
+                    ldsm_x4(bb, cK + box_chunk(C, 16 * pw + (lane & 7) + ((lane >> 4) << 3),
+                                               2 * ks + ((lane >> 3) & 1)));
 #pragma unroll
                 for (int u = 0; u < TPW; ++u) {
-                    const int tile = pw + u * (NTP / 32), j = tile >> 1;
+                    const int tile = tile_of(u), j = tile >> 1;
                     const uint4 *rows = (tile & 1) ? cQ : cK;
-                    unsigned a[4], bb[4];
+                    unsigned a[4];
                     ldsm_x4(a, rows + box_chunk(C, 16 * j + (lane & 15), 2 * ks + (lane >> 4)));
-                    ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
-                                               2 * ks + ((lane >> 3) & 1)));
+                    if constexpr (TPW != 2)
+                        ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
+                                                   2 * ks + ((lane >> 3) & 1)));
                     const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
                     mma_16816(e[u][0], a, b0);
                     mma_16816(e[u][1], a, b1);
                 }
+            }
 #pragma unroll
             for (int u = 0; u < TPW; ++u) {
-                const int tile = pw + u * (NTP / 32);
+                const int tile = tile_of(u);
                 const int j = tile >> 1, isq = tile & 1;
                 const float *e0 = e[u][0], *e1 = e[u][1];
                 const int tl = 16 * j + (lane & 15);

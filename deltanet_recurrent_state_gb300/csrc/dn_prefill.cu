@@ -432,9 +432,19 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                     const uint4 *rows = (tile & 1) ? cQ : cK;
                     unsigned a[4];
                     ldsm_x4(a, rows + box_chunk(C, 16 * j + (lane & 15), 2 * ks + (lane >> 4)));
-                    if constexpr (TPW != 2)
-                        ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
-                                                   2 * ks + ((lane >> 3) & 1)));
+                    if constexpr (TPW != 2) {
+                        // K_j^T of a K tile is made of its own A fragments (tokens 0-7: a[0],
+                        // a[2]; tokens 8-15: a[1], a[3]); a Q tile loads it
+                        if (tile & 1) {
+                            ldsm_x4(bb, cK + box_chunk(C, 16 * j + (lane & 7) + ((lane >> 4) << 3),
+                                                       2 * ks + ((lane >> 3) & 1)));
+                        } else {
+                            bb[0] = a[0];
+                            bb[1] = a[2];
+                            bb[2] = a[1];
+                            bb[3] = a[3];
+                        }
+                    }
                     const unsigned b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
                     mma_16816(e[u][0], a, b0);
                     mma_16816(e[u][1], a, b1);

@@ -487,12 +487,17 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
                     *reinterpret_cast<float2 *>(sA + a_index(j, fr + 8, fc)) = make_float2(a1[0], a1[1]);
                     *reinterpret_cast<float2 *>(sA + a_index(j, fr + 8, fc + 8)) = make_float2(a1[2], a1[3]);
                 } else {
+                    float m0[4], m1[4];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        sMq[pb][j][fr][cs[w]] = __float2half_rn((cs[w] <= fr) ? __expf(Gr0 - Gc[w]) * v0[w] : 0.f);
-                        sMq[pb][j][fr + 8][cs[w]] =
-                            __float2half_rn((cs[w] <= fr + 8) ? __expf(Gr1 - Gc[w]) * v1[w] : 0.f);
+                        m0[w] = (cs[w] <= fr) ? __expf(Gr0 - Gc[w]) * v0[w] : 0.f;
+                        m1[w] = (cs[w] <= fr + 8) ? __expf(Gr1 - Gc[w]) * v1[w] : 0.f;
                     }
+                    // columns (fc, fc + 1) and (fc + 8, fc + 9) as fp16 pairs
+                    *reinterpret_cast<unsigned *>(&sMq[pb][j][fr][fc]) = pack_h2(m0[0], m0[1]);
+                    *reinterpret_cast<unsigned *>(&sMq[pb][j][fr][fc + 8]) = pack_h2(m0[2], m0[3]);
+                    *reinterpret_cast<unsigned *>(&sMq[pb][j][fr + 8][fc]) = pack_h2(m1[0], m1[1]);
+                    *reinterpret_cast<unsigned *>(&sMq[pb][j][fr + 8][fc + 8]) = pack_h2(m1[2], m1[3]);
                 }
             }
             bar_sync(kBarPrep, NTP);
@@ -609,7 +614,8 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {  // R = V^T - gam X_K ; O starts at gam X_Q
                     const int t = 16 * j + 8 * nt + fc;
-                    const float ga = gam[t], gb = gam[t + 1];
+                    const float2 gg = *reinterpret_cast<const float2 *>(gam + t);  // t even
+                    const float ga = gg.x, gb = gg.y;
                     const float2 lo = unpack_h2(vt[2 * nt]), hi = unpack_h2(vt[2 * nt + 1]);
                     R[nt][0] = lo.x - ga * X[mt][nt][0];
                     R[nt][1] = lo.y - gb * X[mt][nt][1];
@@ -643,7 +649,8 @@ prefill_wy_kernel(int H, int P, const __grid_constant__ PrefillMaps maps,
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int t = 16 * j + 8 * nt + fc;
-                    const float da = dec[t], db = dec[t + 1];
+                    const float2 dd = *reinterpret_cast<const float2 *>(dec + t);  // t even
+                    const float da = dd.x, db = dd.y;
                     Dt[nt][0] = Dl[nt][0] * da;
                     Dt[nt][1] = Dl[nt][1] * db;
                     Dt[nt][2] = Dl[nt][2] * da;

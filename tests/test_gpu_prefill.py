@@ -142,6 +142,31 @@ def test_whole_and_half_row_ctas_agree(cuda):
     assert_close("state_out", s_all[:1, heads], ref[2], TOL["f16"])
 
 
+@pytest.mark.parametrize("extra", [10, 100])
+def test_folded_launch_tail_agrees_with_single_sequences(extra, cuda):
+    # N*H = SMs + extra pairs: a folded launch (one full-height CTA a pair) whose last wave is
+    # partial. Each sequence must equal its own single-sequence launch (half-height CTAs) bit
+    # for bit, and its last pair the oracle.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, P, H, d = (sms + extra) // 2, 130, 2, 128
+    x = inputs.recurrence_inputs(N, P, H, d, d, seed=640 + extra, device=cuda)
+    o_all, c_all, s_all = dn.dn_prefill_checkpoint(*[x[k] for k in KEYS], x["state"])
+    torch.cuda.synchronize()
+    assert dn.dn_prefill_wait_timeouts() == 0
+    for n in range(N):
+        xs = [x[k][n:n + 1].contiguous() for k in KEYS]
+        o1, c1, s1 = dn.dn_prefill_checkpoint(*xs, x["state"][n:n + 1].contiguous())
+        assert torch.equal(o1, o_all[n:n + 1]) and torch.equal(c1, c_all[n:n + 1]), n
+        assert torch.equal(s1, s_all[n:n + 1]), n
+    last = N - 1
+    u = {k: np64(x[k][last:]) for k in KEYS}
+    ref = oracle.prefill_checkpoint(u["q"], u["k"], u["v"], u["beta"], u["g"], np64(x["state"][last:]),
+                                    chunk=64, store="f16", io="f16")
+    assert_close("out", o_all[last:], ref[0], TOL["f16"])
+    assert_close("ckpt", c_all[last:], ref[1], TOL["f16"])
+    assert_close("state_out", s_all[last:], ref[2], TOL["f16"])
+
+
 # ---------------------------------------------------------------------------- tcgen05 engine
 
 @pytest.mark.parametrize("P", [0, 1, 15, 63, 64, 65, 129, 200])

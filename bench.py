@@ -528,6 +528,15 @@ def prefill_row(device, stream, reps=2):
             "algorithmic_bytes": nbytes}
 
 
+def add_prefill_fractions(row, hbm):
+    """Both prefill launch forms as fractions of the measured copy peak and of 8 TB/s."""
+    for form in ("per_layer_launches", "folded_one_launch"):
+        r = row[form]
+        r["frac"] = r["achieved_gbs"] / hbm
+        r["frac_of_nominal_8tbs"] = r["achieved_gbs"] / 8000.0
+    return row
+
+
 def deltas_row(sets, device, stream, steps=200, warmup=5):
     """The single-user step with recompute on commit: verify without checkpoints (delta_t
     per row instead), greedy accept, commit rebuilding the accepted state from delta."""
@@ -969,6 +978,8 @@ def main():
         return
 
     hbm, peak_kind = peaks()
+    if "prefill" in rows:
+        add_prefill_fractions(rows["prefill"], hbm)
     vb = verify_bytes(N, T, H, dk, dv, 2)
     ab = accept_bytes(B, T, w["V"], 2)
     cb = commit_bytes(w["L"], sets[0]["acc_plan"], H, dk, dv, 2)

@@ -117,3 +117,11 @@ def test_e2e_growing_groups_cover_the_layers():
         g = bench.e2e_growing_groups(L)
         assert sum(g) == L and min(g) >= 1
         assert bench.e2e_group_bounds(L, g)[-1] == L
+
+
+def test_prefill_fractions_against_both_peaks():
+    row = {"per_layer_launches": {"achieved_gbs": 2000.0}, "folded_one_launch": {"achieved_gbs": 4400.0}}
+    bench.add_prefill_fractions(row, 6775.9)
+    assert abs(row["folded_one_launch"]["frac"] - 4400.0 / 6775.9) < 1e-12
+    assert abs(row["folded_one_launch"]["frac_of_nominal_8tbs"] - 0.55) < 1e-12
+    assert abs(row["per_layer_launches"]["frac"] - 2000.0 / 6775.9) < 1e-12

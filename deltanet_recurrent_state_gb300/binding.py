@@ -95,6 +95,13 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+def _require(cond, what):
+    """Argument check that survives python -O: the C ABI receives raw pointers and cannot
+    see a tensor's size, so a wrong shape must stop here."""
+    if not cond:
+        raise ValueError(what)
+
+
 def _dev(*ts):
     for t in ts:
         if t is not None:
@@ -116,11 +123,13 @@ def dn_verify_block(q, k, v, beta, g, state_in, out=None, ckpt=None, stream=None
     if ckpt is None:
         ckpt = torch.empty((N, T, H, dv, dk), dtype=state_in.dtype, device=q.device)
     _dev(q, k, v, beta, g, state_in, out, ckpt)
-    assert k.shape == q.shape and v.shape == (N, T, H, dv)
-    assert beta.shape == (N, T, H) and g.shape == (N, T, H)
-    assert beta.dtype == torch.float32 and g.dtype == torch.float32
-    assert state_in.shape == (N, H, dv, dk) and ckpt.shape == (N, T, H, dv, dk)
-    assert out.shape == (N, T, H, dv) and out.dtype == q.dtype and ckpt.dtype == state_in.dtype
+    _require(k.shape == q.shape and v.shape == (N, T, H, dv), "k like q, v [N,T,H,dv]")
+    _require(beta.shape == (N, T, H) and g.shape == (N, T, H), "beta, g [N,T,H]")
+    _require(beta.dtype == torch.float32 and g.dtype == torch.float32, "beta, g fp32")
+    _require(state_in.shape == (N, H, dv, dk) and ckpt.shape == (N, T, H, dv, dk),
+             "state_in [N,H,dv,dk], ckpt [N,T,H,dv,dk]")
+    _require(out.shape == (N, T, H, dv) and out.dtype == q.dtype and ckpt.dtype == state_in.dtype,
+             "out [N,T,H,dv] in q's dtype, ckpt in the state's")
     st = load_library().dn_verify_block(
         N, H, T, dk, dv, _DT[q.dtype], _DT[state_in.dtype], _ptr(q), _ptr(k), _ptr(v),
         _ptr(beta), _ptr(g), _ptr(state_in), _ptr(out), _ptr(ckpt), _stream(stream))
@@ -137,8 +146,9 @@ def dn_verify_block_deltas(q, k, v, beta, g, state_in, out=None, delta=None, str
     if delta is None:
         delta = torch.empty((N, T, H, dv), dtype=torch.float32, device=q.device)
     _dev(q, k, v, beta, g, state_in, out, delta)
-    assert k.shape == q.shape and v.shape == (N, T, H, dv) and state_in.shape == (N, H, dv, dk)
-    assert delta.shape == (N, T, H, dv) and delta.dtype == torch.float32
+    _require(k.shape == q.shape and v.shape == (N, T, H, dv) and state_in.shape == (N, H, dv, dk),
+             "k like q, v [N,T,H,dv], state_in [N,H,dv,dk]")
+    _require(delta.shape == (N, T, H, dv) and delta.dtype == torch.float32, "delta [N,T,H,dv] fp32")
     st = load_library().dn_verify_block_deltas(
         N, H, T, dk, dv, _DT[q.dtype], _DT[state_in.dtype], _ptr(q), _ptr(k), _ptr(v),
         _ptr(beta), _ptr(g), _ptr(state_in), _ptr(out), _ptr(delta), _stream(stream))
@@ -152,7 +162,8 @@ def dn_commit_deltas(k, g, delta, accepted_len, state, stream=None):
     T = k.shape[1]
     B = accepted_len.shape[0]
     _dev(k, g, delta, accepted_len, state)
-    assert k.shape == (N, T, H, dk) and g.shape == (N, T, H) and delta.shape == (N, T, H, dv)
+    _require(k.shape == (N, T, H, dk) and g.shape == (N, T, H) and delta.shape == (N, T, H, dv),
+             "k [N,T,H,dk], g [N,T,H], delta [N,T,H,dv]")
     st = load_library().dn_commit_deltas(N, B, H, T, dk, dv, _DT[state.dtype], _ptr(k), _ptr(g),
                                          _ptr(delta), _ptr(accepted_len), _ptr(state),
                                          _stream(stream))
@@ -182,8 +193,8 @@ def dn_accept_greedy(logits, draft_ids, target_ids=None, accepted_len=None, work
     if workspace is None:
         workspace = accept_workspace(B, T, V, dev)
     _dev(logits, draft_ids, target_ids, accepted_len, workspace)
-    assert draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32
-    assert target_ids.shape == (B, T) and accepted_len.shape == (B,)
+    _require(draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32, "draft_ids [B,T] int32")
+    _require(target_ids.shape == (B, T) and accepted_len.shape == (B,), "target_ids [B,T], accepted_len [B]")
     st = load_library().dn_accept_greedy(
         B, T, V, _DT[logits.dtype], _ptr(logits), _ptr(draft_ids), _ptr(target_ids),
         _ptr(accepted_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -200,9 +211,9 @@ def dn_accept_greedy_noalloc(logits, draft_ids, target_ids, accepted_len, stream
     """
     B, T, V = logits.shape
     _dev(logits, draft_ids, target_ids, accepted_len)
-    assert draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32
-    assert target_ids.shape == (B, T) and target_ids.dtype == torch.int32
-    assert accepted_len.shape == (B,) and accepted_len.dtype == torch.int32
+    _require(draft_ids.shape == (B, T) and draft_ids.dtype == torch.int32, "draft_ids [B,T] int32")
+    _require(target_ids.shape == (B, T) and target_ids.dtype == torch.int32, "target_ids [B,T] int32")
+    _require(accepted_len.shape == (B,) and accepted_len.dtype == torch.int32, "accepted_len [B] int32")
     st = load_library().dn_accept_greedy_noalloc(
         B, T, V, _DT[logits.dtype], _ptr(logits), _ptr(draft_ids), _ptr(target_ids),
         _ptr(accepted_len), _stream(stream))
@@ -216,8 +227,8 @@ def dn_commit(ckpt, accepted_len, state, stream=None):
     T = ckpt.shape[1]
     B = accepted_len.shape[0]
     _dev(ckpt, accepted_len, state)
-    assert ckpt.shape == (N, T, H, dv, dk) and ckpt.dtype == state.dtype
-    assert accepted_len.dtype == torch.int32
+    _require(ckpt.shape == (N, T, H, dv, dk) and ckpt.dtype == state.dtype, "ckpt [N,T,H,dv,dk] in the state's dtype")
+    _require(accepted_len.dtype == torch.int32, "accepted_len int32")
     st = load_library().dn_commit(N, B, H, T, dk, dv, _DT[state.dtype], _ptr(ckpt),
                                   _ptr(accepted_len), _ptr(state), _stream(stream))
     _check("dn_commit", st)
@@ -242,9 +253,12 @@ def dn_prefill_checkpoint(q, k, v, beta, g, state_in=None, out=None, ckpt=None, 
     if state_out is None:
         state_out = torch.empty((N, H, dv, dk), dtype=sdt, device=dev)
     _dev(q, k, v, beta, g, state_in, out, ckpt, state_out)
-    assert k.shape == q.shape and v.shape == (N, P, H, dv) and beta.shape == (N, P, H)
-    assert g.shape == (N, P, H) and out.shape == (N, P, H, dv)
-    assert ckpt.shape == (N, P // chunk, H, dv, dk) and state_out.shape == (N, H, dv, dk)
+    _require(k.shape == q.shape and v.shape == (N, P, H, dv) and beta.shape == (N, P, H),
+             "k like q, v [N,P,H,dv], beta [N,P,H]")
+    _require(g.shape == (N, P, H) and out.shape == (N, P, H, dv), "g [N,P,H], out [N,P,H,dv]")
+    _require(beta.dtype == torch.float32 and g.dtype == torch.float32, "beta and g are fp32")
+    _require(ckpt.shape == (N, P // chunk, H, dv, dk) and state_out.shape == (N, H, dv, dk),
+             "ckpt [N,P/chunk,H,dv,dk], state_out [N,H,dv,dk]")
     name = {"mma": "dn_prefill_checkpoint", "tc": "dn_prefill_checkpoint_tc"}[engine]
     st = getattr(load_library(), name)(
         N, H, P, chunk, dk, dv, _DT[q.dtype], _DT[sdt], _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
@@ -281,8 +295,10 @@ def dn_context_drafts(context, lengths, n_max=4, n_min=1, K=8, drafts=None, coun
     if match_len is None:
         match_len = torch.empty((N,), dtype=torch.int32, device=dev)
     _dev(context, lengths, drafts, count, match_len)
-    assert context.dtype == lengths.dtype == drafts.dtype == count.dtype == torch.int32
-    assert lengths.shape == (N,) and drafts.shape == (N, K) and count.shape == (N,)
+    _require(context.dtype == lengths.dtype == drafts.dtype == count.dtype == torch.int32,
+             "context, lengths, drafts, count int32")
+    _require(lengths.shape == (N,) and drafts.shape == (N, K) and count.shape == (N,),
+             "lengths [N], drafts [N,K], count [N]")
     st = load_library().dn_context_drafts(N, stride, n_max, n_min, K, _ptr(context), _ptr(lengths),
                                           _ptr(drafts), _ptr(count), _ptr(match_len),
                                           _stream(stream))

@@ -167,6 +167,19 @@ def test_folded_launch_tail_agrees_with_single_sequences(extra, cuda):
     assert_close("state_out", s_all[last:], ref[2], TOL["f16"])
 
 
+def test_binding_rejects_wrong_shapes_and_dtypes(cuda):
+    # The C ABI takes raw pointers and cannot see sizes: the binding stops a mis-sized or
+    # mis-typed tensor with ValueError (not an assert that python -O would strip).
+    x = inputs.recurrence_inputs(1, 70, 2, 64, 64, seed=5, device=cuda)
+    base = [x[k] for k in KEYS]
+    with pytest.raises(ValueError):
+        dn.dn_prefill_checkpoint(*base[:3], x["beta"][:, :-1].contiguous(), x["g"], x["state"])
+    with pytest.raises(ValueError):
+        dn.dn_prefill_checkpoint(*base[:3], x["beta"].half(), x["g"], x["state"])
+    with pytest.raises(ValueError):
+        dn.dn_prefill_checkpoint(*base, x["state"], out=torch.empty(1, 69, 2, 64, dtype=x["q"].dtype, device=cuda))
+
+
 # ---------------------------------------------------------------------------- tcgen05 engine
 
 @pytest.mark.parametrize("P", [0, 1, 15, 63, 64, 65, 129, 200])

@@ -737,14 +737,13 @@ dn_status launch_prefill_wy_split(int N, int H, int P, const void *q, const void
                                   const float *beta, const float *g, const void *s_in, void *out,
                                   void *ckpt, void *s_out, cudaStream_t st) {
     constexpr size_t bytes = PrefillSmem<DK, DVC>::kBytes;
-    static bool configured = false;  // the attribute is per function and idempotent
-    if (!configured) {
-        if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, DVC, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)bytes) != cudaSuccess) {
-            cudaGetLastError();
-            return DN_ERR_CUDA;
-        }
-        configured = true;
+    // Set on every launch (a host call of about a microsecond): the attribute belongs to the
+    // current device's context, and a flag cached across calls would race between host
+    // threads and miss a second device.
+    if (cudaFuncSetAttribute(prefill_wy_kernel<DK, DV, DVC, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return DN_ERR_CUDA;
     }
     PrefillMaps maps;
     memset(&maps, 0, sizeof(maps));
